@@ -1,0 +1,369 @@
+#!/usr/bin/env python
+"""Benchmark: DDTree verify attention (MLA absorbed, page_size=1) on one GB300.
+
+Default workload: Long TP8-slice, 65,536-token prefix, 32-node random tree,
+8 heads, scattered indices into a 262,144-row pool (the 65k-prefix headline).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Per step: an L2 flush (a write of 2x the L2 size, outside the timed events),
+then one verify call replayed from a CUDA graph captured on an explicit
+stream.  The call's device time, and the split-KV partial kernel's own time
+(events the library records between its kernels), are taken with CUDA
+events.  Rank 0 prints one JSON line.  N > 1 runs independent replicas (the
+call does not shard across GPUs here), each rank on its own GPU.
+
+--impl reference times the float64 CPU oracle on the host cores for the same
+workload and metric (it is the only reference implementation this repo has).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "verify-attn µs/call & achieved HBM GB/s at 65k prefix; % of roofline"
+UNIT = "us/call"
+
+
+def _args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=30)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="long_scattered")
+    ap.add_argument("--kernel", choices=["auto", "simt", "tc"], default="auto")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-contiguous", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    return ap.parse_args()
+
+
+def _dist():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    return world, rank, local
+
+
+def _barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def _max_over_ranks(world, x: float) -> float:
+    if world == 1:
+        return x
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def _peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            p = json.load(f)
+        return dict(hbm_gbs=float(p["hbm_gbs"]), bf16_tflops=float(p["bf16_tflops"]),
+                    bf16_tflops_sustained=float(p.get("bf16_tflops_sustained", p["bf16_tflops"])),
+                    source="measured")
+    return dict(hbm_gbs=6800.0, bf16_tflops=1900.0, bf16_tflops_sustained=1700.0, source="fallback")
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle-reason samples while the timed region runs."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.proc = None
+        self.idx = device_index
+        self.out = os.path.join("/tmp", f"ddtree_clocks_{os.getpid()}.csv")
+
+    def __enter__(self):
+        try:
+            self.f = open(self.out, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-i", str(self.idx), "-lms", "100"], stdout=self.f, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+            self.f.close()
+
+    def summary(self):
+        if self.proc is None or not os.path.exists(self.out):
+            return None
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in open(self.out):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def _pct(xs, q):
+    xs = sorted(xs)
+    k = (len(xs) - 1) * q
+    lo, hi = math.floor(k), math.ceil(k)
+    return xs[lo] + (xs[hi] - xs[lo]) * (k - lo)
+
+
+def run_reference(args, world, rank):
+    """Float64 CPU oracle on the host cores, same workload/metric/unit."""
+    if rank != 0:
+        return
+    from oracle import verify_batched
+    from speculative_decode_tree_gb300.workloads import algorithmic_cost, workload
+    inp = workload(args.workload)
+    cost = algorithmic_cost(inp)
+    cores = torch.get_num_threads()
+
+    def step():
+        t0 = time.perf_counter()
+        verify_batched(inp.q_latent, inp.q_rope, inp.kv_pool, inp.kv_indices, inp.kv_indptr,
+                       inp.prefix_lens, inp.tree_parent, inp.sm_scale)
+        return time.perf_counter() - t0
+
+    for _ in range(args.warmup):
+        step()
+    ts = [step() for _ in range(args.steps)]
+    us = statistics.median(ts) * 1e6
+    line = {
+        "impl": "reference", "metric": METRIC, "value": us, "unit": UNIT, "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": statistics.mean(ts) * 1e3,
+        "higher_is_better": False, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "config": {"workload": args.workload, "batch": inp.batch,
+                                        "heads": inp.n_heads, "nodes": inp.n_nodes,
+                                        "prefixes": inp.prefix_lens.tolist(), "pool_rows": inp.pool_rows},
+        "gbs": cost["bytes"] / (us * 1e-6) / 1e9, "tflops": cost["flops"] / (us * 1e-6) / 1e12,
+        "cpu_baseline": {"value": us, "unit": UNIT, "cores": cores, "kind": "oracle",
+                         "sample": f"full {args.workload} call per step, {args.steps} steps"},
+        "e2e": {"value": us, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+    print(json.dumps(line), flush=True)
+
+
+def run_ours(args, world, rank, local):
+    from speculative_decode_tree_gb300 import binding as B
+    from speculative_decode_tree_gb300.build import build
+    from speculative_decode_tree_gb300.runner import DeviceVerify
+    from speculative_decode_tree_gb300.workloads import algorithmic_cost, workload
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if rank == 0 or world == 1:
+        build()
+    _barrier(world)
+    peaks = _peaks()
+    inp = workload(args.workload)
+    cost = algorithmic_cost(inp)
+    kernel = {"auto": None, "simt": B.DDTREE_KERNEL_SIMT, "tc": B.DDTREE_KERNEL_TC}[args.kernel]
+    dv = DeviceVerify(inp, device=str(dev), kernel=kernel)
+    props = torch.cuda.get_device_properties(dev)
+    l2 = getattr(props, "L2_cache_size", 128 << 20) or (128 << 20)
+    flush = torch.empty(2 * l2 // 4 + 1024, dtype=torch.float32, device=dev)
+    stream = torch.cuda.Stream(device=dev)
+    stage = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    for e in stage + [t0, t1]:  # torch creates the CUDA event on its first record
+        e.record(stream)
+    assert all(e.cuda_event for e in stage)
+
+    with torch.cuda.stream(stream):
+        dv.run_timed(stage)  # first call outside capture (kernel attributes)
+    stream.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream):
+        dv.run_timed(stage)
+
+    def one_step():
+        with torch.cuda.stream(stream):
+            flush.zero_()
+            t0.record(stream)
+            graph.replay()
+            t1.record(stream)
+        stream.synchronize()
+        return t0.elapsed_time(t1) * 1e3, stage[0].elapsed_time(stage[1]) * 1e3, \
+            stage[1].elapsed_time(stage[2]) * 1e3
+
+    for _ in range(args.warmup):
+        one_step()
+    _barrier(world)
+    torch.cuda.synchronize()
+    calls, partials, combines = [], [], []
+    with ClockSampler(local) as clk:
+        wall0 = time.perf_counter()
+        for _ in range(args.steps):
+            c, p, m = one_step()
+            calls.append(c)
+            partials.append(p)
+            combines.append(m)
+        torch.cuda.synchronize()
+        _barrier(world)
+        wall = time.perf_counter() - wall0
+    status = dv.status(stream)
+
+    call_us = _max_over_ranks(world, statistics.median(calls))
+    mean_call_us = _max_over_ranks(world, statistics.mean(calls))
+    partial_us = _max_over_ranks(world, statistics.mean(partials))
+    value = call_us / world  # replicas: calls of the whole job per unit time
+
+    # The same call against the defragmented (contiguous) copy of the pool.
+    contiguous_us = None
+    if args.workload == "long_scattered" and not args.no_contiguous:
+        dvc = DeviceVerify(workload("long_contiguous"), device=str(dev), kernel=kernel)
+        gc = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(stream):
+            dvc.run()
+        stream.synchronize()
+        with torch.cuda.graph(gc, stream=stream):
+            dvc.run()
+        cs = []
+        for i in range(args.warmup + args.steps):
+            with torch.cuda.stream(stream):
+                flush.zero_()
+                t0.record(stream)
+                gc.replay()
+                t1.record(stream)
+            stream.synchronize()
+            if i >= args.warmup:
+                cs.append(t0.elapsed_time(t1) * 1e3)
+        contiguous_us = statistics.median(cs)
+        del dvc, gc
+
+    # End to end through the C ABI with host buffers: pinned H2D of the step's
+    # inputs (queries, indices, parents, lengths) and D2H of out + lse.
+    e2e = None
+    if not args.no_e2e:
+        host_in = [t.pin_memory() for t in (inp.q_latent, inp.q_rope, inp.kv_indices, inp.kv_indptr,
+                                            inp.prefix_lens, inp.tree_parent)]
+        dev_in = [dv.q_latent, dv.q_rope, dv.kv_indices, dv.kv_indptr, dv.prefix_lens, dv.tree_parent]
+        host_out = [torch.empty_like(dv.out, device="cpu").pin_memory(),
+                    torch.empty_like(dv.lse, device="cpu").pin_memory()]
+        h2d = sum(t.numel() * t.element_size() for t in host_in)
+        d2h = sum(t.numel() * t.element_size() for t in host_out)
+        es = []
+        for i in range(args.warmup + args.steps):
+            with torch.cuda.stream(stream):
+                flush.zero_()
+                t0.record(stream)
+                for h, d in zip(host_in, dev_in):
+                    d.copy_(h, non_blocking=True)
+                dv.run(stream)
+                host_out[0].copy_(dv.out, non_blocking=True)
+                host_out[1].copy_(dv.lse, non_blocking=True)
+                t1.record(stream)
+            stream.synchronize()
+            if i >= args.warmup:
+                es.append(t0.elapsed_time(t1) * 1e3)
+        e2e_us = _max_over_ranks(world, statistics.median(es)) / world
+        e2e = {"value": e2e_us, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        from oracle import verify_batched
+        ts = []
+        tstart = time.perf_counter()
+        while not ts or time.perf_counter() - tstart < args.cpu_seconds:
+            a = time.perf_counter()
+            verify_batched(inp.q_latent, inp.q_rope, inp.kv_pool, inp.kv_indices, inp.kv_indptr,
+                           inp.prefix_lens, inp.tree_parent, inp.sm_scale)
+            ts.append(time.perf_counter() - a)
+        cpu = {"value": statistics.median(ts) * 1e6, "unit": UNIT, "cores": torch.get_num_threads(),
+               "kind": "oracle",
+               "sample": f"{len(ts)} full {args.workload} calls (float64, torch CPU), median"}
+
+    if rank != 0:
+        return
+    flops, byts = cost["flops"], cost["bytes"]
+    tc_peak = peaks["bf16_tflops"]
+    achieved = flops / (partial_us * 1e-6) / 1e12
+    roof_us = max(byts / (peaks["hbm_gbs"] * 1e9), flops / (tc_peak * 1e12)) * 1e6
+    clocks = clk.summary()
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": mean_call_us / 1e3, "higher_is_better": False,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": args.workload, "batch": inp.batch, "heads": inp.n_heads,
+                   "nodes": inp.n_nodes, "prefixes": inp.prefix_lens.tolist(),
+                   "pool_rows": inp.pool_rows, "index_mode": inp.meta["index_mode"],
+                   "l2": "flushed between steps (2x L2 write, outside the timed events)",
+                   "timing": "CUDA graph replay on an explicit stream; CUDA events",
+                   "parallelism": "replicas" if world > 1 else "single GPU"},
+        "p10_us": _pct(calls, 0.1), "p90_us": _pct(calls, 0.9),
+        "gbs": byts / (call_us * 1e-6) / 1e9,
+        "tflops": flops / (call_us * 1e-6) / 1e12,
+        "roofline_us": roof_us, "roofline_frac_call": roof_us / call_us,
+        "partial_kernel_us": partial_us, "combine_kernel_us": statistics.mean(combines),
+        "roofline": {"bound": "tensor", "achieved": achieved, "peak": tc_peak, "unit": "TFLOP/s",
+                     "frac": achieved / tc_peak, "traffic": None,
+                     "peak_source": peaks["source"] + " bf16 burst (MEASURED_PEAKS.json)",
+                     "kernel": "split-KV partial (%s)" % ("tcgen05" if dv.plan.kernel == 2 else "simt")},
+        "alg_bytes": byts, "alg_flops": flops,
+        "plan": dv.plan.as_dict(),
+        "contiguous_us": contiguous_us,
+        "scatter_over_contiguous": (call_us / contiguous_us) if contiguous_us else None,
+        "cpu_baseline": cpu, "e2e": e2e, "clocks": clocks,
+        "gpu_launches": 2 * args.steps,
+        "status_word": status, "wall_s_timed_region": wall,
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    args = _args()
+    world, rank, local = _dist()
+    try:
+        if args.impl == "reference":
+            run_reference(args, world, rank)
+        else:
+            run_ours(args, world, rank, local)
+    finally:
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

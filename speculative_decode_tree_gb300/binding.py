@@ -1,0 +1,208 @@
+"""Thin Python binding of the C ABI in include/ddtree_verify.h.
+
+Argument marshalling only: tensors become device pointers, the current torch
+stream becomes the cudaStream_t, return codes become exceptions.  Every step
+of the verify path runs in the library's CUDA kernels; there is no CPU
+fallback, and loading fails loudly when the library has not been built.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional, Sequence
+
+import torch
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(HERE, "_lib", "libddtree_verify.so")
+
+DDTREE_OK = 0
+DDTREE_EINVAL = 1
+DDTREE_EWORKSPACE = 2
+DDTREE_EUNSUPPORTED = 3
+DDTREE_ELAUNCH = 4
+DDTREE_EDEVICE_DATA = 5
+DDTREE_ECUDA = 6
+
+DDTREE_ST_BAD_INDEX = 0x1
+DDTREE_ST_BAD_PARENT = 0x2
+DDTREE_ST_BAD_LENGTH = 0x4
+DDTREE_ST_TIMEOUT = 0x8
+
+DDTREE_KERNEL_AUTO = 0
+DDTREE_KERNEL_SIMT = 1
+DDTREE_KERNEL_TC = 2
+
+EXPORTS = (
+    "ddtree_verify_mla_plan", "ddtree_verify_mla_plan_ex", "ddtree_verify_mla_workspace_size",
+    "ddtree_verify_mla", "ddtree_verify_mla_batched", "ddtree_build_ancestor_mask",
+    "ddtree_verify_mla_check", "ddtree_status_str", "ddtree_verify_mla_batched_timed",
+)
+
+
+class Plan(ctypes.Structure):
+    _fields_ = [
+        ("batch", ctypes.c_int32), ("n_nodes", ctypes.c_int32), ("n_heads", ctypes.c_int32),
+        ("rows_per_req", ctypes.c_int32), ("pool_rows", ctypes.c_int64),
+        ("max_keys", ctypes.c_int32), ("kernel", ctypes.c_int32), ("tile_keys", ctypes.c_int32),
+        ("chunk_keys", ctypes.c_int32), ("total_splits", ctypes.c_int32),
+        ("row_tile", ctypes.c_int32), ("row_tiles", ctypes.c_int32), ("num_sms", ctypes.c_int32),
+        ("q_latent_row_stride", ctypes.c_int32), ("q_rope_row_stride", ctypes.c_int32),
+        ("workspace_bytes", ctypes.c_int64), ("off_partial_lse", ctypes.c_int64),
+        ("off_partial_o", ctypes.c_int64), ("reserved", ctypes.c_int32 * 8),
+    ]
+
+    def as_dict(self) -> dict:
+        return {k: getattr(self, k) for k, _ in self._fields_ if k != "reserved"}
+
+
+class DDTreeError(RuntimeError):
+    def __init__(self, code: int, where: str):
+        self.code = code
+        super().__init__(f"{where}: {code} ({ddtree_status_str(code)})")
+
+
+_lib = None
+
+
+def library() -> ctypes.CDLL:
+    """Load the in-tree library once; raise if it has not been built."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(LIB_PATH):
+        raise RuntimeError(f"CUDA library not built: {LIB_PATH} is missing "
+                           "(run speculative_decode_tree_gb300.build.build())")
+    L = ctypes.CDLL(LIB_PATH)
+    vp, i32, i64, f32, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_float, ctypes.c_size_t
+    P = ctypes.POINTER(Plan)
+    L.ddtree_verify_mla_plan.argtypes = [i32, i32, i32, vp, i64, P]
+    L.ddtree_verify_mla_plan_ex.argtypes = [i32, i32, i32, vp, i64, i32, i32, P]
+    L.ddtree_verify_mla_workspace_size.argtypes = [P]
+    L.ddtree_verify_mla_workspace_size.restype = sz
+    L.ddtree_verify_mla.argtypes = [vp, vp, vp, vp, i32, vp, i32, i32, f32, vp, vp, vp, vp]
+    L.ddtree_verify_mla_batched.argtypes = [P, vp, vp, vp, vp, vp, vp, vp, f32, vp, vp, vp, sz, vp]
+    L.ddtree_verify_mla_batched_timed.argtypes = [P, vp, vp, vp, vp, vp, vp, vp, f32, vp, vp, vp, sz,
+                                                  vp, vp]
+    L.ddtree_build_ancestor_mask.argtypes = [vp, i32, i32, vp, vp, vp]
+    L.ddtree_verify_mla_check.argtypes = [vp, vp, ctypes.POINTER(ctypes.c_uint32)]
+    L.ddtree_status_str.argtypes = [i32]
+    L.ddtree_status_str.restype = ctypes.c_char_p
+    for name in ("ddtree_verify_mla_plan", "ddtree_verify_mla_plan_ex", "ddtree_verify_mla",
+                 "ddtree_verify_mla_batched", "ddtree_build_ancestor_mask", "ddtree_verify_mla_check",
+                 "ddtree_verify_mla_batched_timed"):
+        getattr(L, name).restype = i32
+    _lib = L
+    return L
+
+
+def _ptr(t: Optional[torch.Tensor]) -> Optional[int]:
+    return None if t is None else t.data_ptr()
+
+
+def _dev(t: torch.Tensor, dtype: torch.dtype, name: str) -> int:
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise TypeError(f"{name} must be a CUDA tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    return t.data_ptr()
+
+
+def _stream(stream) -> int:
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def _check(rc: int, where: str) -> None:
+    if rc != DDTREE_OK:
+        raise DDTreeError(rc, where)
+
+
+def ddtree_status_str(code: int) -> str:
+    return library().ddtree_status_str(int(code)).decode()
+
+
+def ddtree_verify_mla_plan(batch: int, n_nodes: int, n_heads: int, prefix_lens: Sequence[int],
+                           pool_rows: int) -> Plan:
+    arr = (ctypes.c_int32 * max(len(prefix_lens), 1))(*[int(p) for p in prefix_lens])
+    plan = Plan()
+    _check(library().ddtree_verify_mla_plan(batch, n_nodes, n_heads, ctypes.cast(arr, ctypes.c_void_p),
+                                            int(pool_rows), ctypes.byref(plan)), "plan")
+    return plan
+
+
+def ddtree_verify_mla_plan_ex(batch: int, n_nodes: int, n_heads: int, prefix_lens: Sequence[int],
+                              pool_rows: int, num_sms: int, kernel: int = DDTREE_KERNEL_AUTO) -> Plan:
+    arr = (ctypes.c_int32 * max(len(prefix_lens), 1))(*[int(p) for p in prefix_lens])
+    plan = Plan()
+    _check(library().ddtree_verify_mla_plan_ex(batch, n_nodes, n_heads, ctypes.cast(arr, ctypes.c_void_p),
+                                               int(pool_rows), int(num_sms), int(kernel),
+                                               ctypes.byref(plan)), "plan_ex")
+    return plan
+
+
+def ddtree_verify_mla_workspace_size(plan: Plan) -> int:
+    return int(library().ddtree_verify_mla_workspace_size(ctypes.byref(plan)))
+
+
+def ddtree_verify_mla(q_latent, q_rope, kv_pool, kv_indices, prefix_len: int, tree_parent,
+                      n_nodes: int, n_heads: int, sm_scale: float, out, lse, workspace,
+                      stream=None) -> None:
+    bf, i32 = torch.bfloat16, torch.int32
+    rc = library().ddtree_verify_mla(
+        _dev(q_latent, bf, "q_latent"), _dev(q_rope, bf, "q_rope"), _dev(kv_pool, bf, "kv_pool"),
+        _dev(kv_indices, i32, "kv_indices"), int(prefix_len), _dev(tree_parent, i32, "tree_parent"),
+        int(n_nodes), int(n_heads), float(sm_scale), _dev(out, bf, "out"),
+        _dev(lse, torch.float32, "lse"), _dev(workspace, torch.uint8, "workspace"), _stream(stream))
+    _check(rc, "ddtree_verify_mla")
+
+
+def ddtree_verify_mla_batched(plan: Plan, q_latent, q_rope, kv_pool, kv_indices, kv_indptr,
+                              prefix_lens, tree_parent, sm_scale: float, out, lse, workspace,
+                              stream=None) -> None:
+    bf, i32 = torch.bfloat16, torch.int32
+    rc = library().ddtree_verify_mla_batched(
+        ctypes.byref(plan), _dev(q_latent, bf, "q_latent"), _dev(q_rope, bf, "q_rope"),
+        _dev(kv_pool, bf, "kv_pool"), _dev(kv_indices, i32, "kv_indices"),
+        _dev(kv_indptr, i32, "kv_indptr"), _dev(prefix_lens, i32, "prefix_lens"),
+        _dev(tree_parent, i32, "tree_parent"), float(sm_scale), _dev(out, bf, "out"),
+        _dev(lse, torch.float32, "lse"), _dev(workspace, torch.uint8, "workspace"),
+        workspace.numel(), _stream(stream))
+    _check(rc, "ddtree_verify_mla_batched")
+
+
+def ddtree_verify_mla_batched_timed(plan: Plan, q_latent, q_rope, kv_pool, kv_indices, kv_indptr,
+                                    prefix_lens, tree_parent, sm_scale: float, out, lse, workspace,
+                                    stage_events, stream=None) -> None:
+    """As ddtree_verify_mla_batched, recording three torch.cuda.Event objects
+    (before the partial kernel, between partial and combine, after combine)."""
+    bf, i32 = torch.bfloat16, torch.int32
+    evs = (ctypes.c_void_p * 3)(*[None if e is None else e.cuda_event for e in stage_events])
+    rc = library().ddtree_verify_mla_batched_timed(
+        ctypes.byref(plan), _dev(q_latent, bf, "q_latent"), _dev(q_rope, bf, "q_rope"),
+        _dev(kv_pool, bf, "kv_pool"), _dev(kv_indices, i32, "kv_indices"),
+        _dev(kv_indptr, i32, "kv_indptr"), _dev(prefix_lens, i32, "prefix_lens"),
+        _dev(tree_parent, i32, "tree_parent"), float(sm_scale), _dev(out, bf, "out"),
+        _dev(lse, torch.float32, "lse"), _dev(workspace, torch.uint8, "workspace"),
+        workspace.numel(), _stream(stream), ctypes.cast(evs, ctypes.c_void_p))
+    _check(rc, "ddtree_verify_mla_batched_timed")
+
+
+def ddtree_build_ancestor_mask(tree_parent, batch: int, n_nodes: int, anc_out, status=None,
+                               stream=None) -> None:
+    rc = library().ddtree_build_ancestor_mask(
+        _dev(tree_parent, torch.int32, "tree_parent"), int(batch), int(n_nodes),
+        _dev(anc_out, torch.int64, "anc_out"),
+        None if status is None else _dev(status, torch.int32, "status"), _stream(stream))
+    _check(rc, "ddtree_build_ancestor_mask")
+
+
+def ddtree_verify_mla_check(workspace, stream=None) -> int:
+    """Synchronising read of the device status word; returns its DDTREE_ST_* bits."""
+    v = ctypes.c_uint32(0)
+    rc = library().ddtree_verify_mla_check(_dev(workspace, torch.uint8, "workspace"), _stream(stream),
+                                           ctypes.byref(v))
+    if rc not in (DDTREE_OK, DDTREE_EDEVICE_DATA):
+        raise DDTreeError(rc, "ddtree_verify_mla_check")
+    return int(v.value)

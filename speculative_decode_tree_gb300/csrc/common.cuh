@@ -1,0 +1,130 @@
+// Shared device-side definitions of the DDTree verify-attention library.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/ddtree_verify.h"
+
+namespace ddtree {
+
+constexpr int kLatent = DDTREE_LATENT_DIM;  // 512: value width
+constexpr int kRope = DDTREE_ROPE_DIM;      // 64
+constexpr int kRow = DDTREE_ROW_DIM;        // 576: key width
+
+// Everything a launch needs, resolved on the host from the plan and the
+// caller's pointers.  Passed by value as a kernel parameter.
+struct VerifyArgs {
+  const uint16_t* q_latent;
+  const uint16_t* q_rope;
+  const uint16_t* kv_pool;
+  const int32_t* kv_indices;
+  const int32_t* kv_indptr;    // null: single request starting at index 0
+  const int32_t* prefix_lens;  // null: single request of length prefix_len_host
+  const int32_t* tree_parent;  // [B, T]
+  uint16_t* out;
+  float* lse;
+  float* partial_lse;          // [total_splits, rows_per_req]
+  float* partial_o;            // [total_splits, rows_per_req, 512]
+  uint32_t* status;            // workspace offset 0
+  int64_t pool_rows;           // <= 0: indices unchecked
+  float sm_scale;
+  int32_t prefix_len_host;
+  int32_t batch, n_nodes, n_heads, rows_per_req;
+  int32_t tile_keys, chunk_keys, total_splits, row_tile, row_tiles;
+  int32_t q_lat_stride, q_rope_stride;
+};
+
+// One work item's request: which request a split slot belongs to, and the
+// request's lengths as read on the device.
+struct SplitLoc {
+  int b;            // request
+  int s;            // split within the request
+  int P;            // prefix length
+  int nkeys;        // P + T
+  int64_t idx_base; // first kv_indices entry of the request
+};
+
+__device__ __forceinline__ int dev_prefix_len(const VerifyArgs& a, int b) {
+  return a.prefix_lens ? __ldg(a.prefix_lens + b) : a.prefix_len_host;
+}
+
+// Maps split slot w to (request, split).  Slots are laid out request by
+// request: request b owns ceil((P_b+T)/chunk) consecutive slots.  Returns
+// false (and flags BAD_LENGTH when lengths are inconsistent) for slots past
+// the last request; the plan sizes total_splits for the longest lengths.
+__device__ __forceinline__ bool locate_split(const VerifyArgs& a, int w, SplitLoc& loc) {
+  int acc = 0;
+  for (int r = 0; r < a.batch; ++r) {
+    int P = dev_prefix_len(a, r);
+    if (P < 0) {
+      atomicOr(a.status, DDTREE_ST_BAD_LENGTH);
+      return false;
+    }
+    int n = P + a.n_nodes;
+    int ns = (n + a.chunk_keys - 1) / a.chunk_keys;
+    if (w < acc + ns) {
+      loc.b = r;
+      loc.s = w - acc;
+      loc.P = P;
+      loc.nkeys = n;
+      loc.idx_base = a.kv_indptr ? (int64_t)__ldg(a.kv_indptr + r) : 0;
+      if (a.kv_indptr && __ldg(a.kv_indptr + r + 1) - __ldg(a.kv_indptr + r) != n) {
+        atomicOr(a.status, DDTREE_ST_BAD_LENGTH);
+        return false;
+      }
+      if (acc + ns > a.total_splits) {  // longer than planned: no slot
+        atomicOr(a.status, DDTREE_ST_BAD_LENGTH);
+        return false;
+      }
+      return true;
+    }
+    acc += ns;
+  }
+  return false;
+}
+
+// First slot and split count of request b (for the combine stage).
+__device__ __forceinline__ void request_slots(const VerifyArgs& a, int b, int& first, int& count) {
+  int acc = 0;
+  for (int r = 0; r < b; ++r) {
+    int P = max(dev_prefix_len(a, r), 0);
+    acc += (P + a.n_nodes + a.chunk_keys - 1) / a.chunk_keys;
+  }
+  int P = max(dev_prefix_len(a, b), 0);
+  first = acc;
+  count = (P + a.n_nodes + a.chunk_keys - 1) / a.chunk_keys;
+}
+
+// Ancestor set of node i as a bitmask: bit j set when j is i or one of its
+// ancestors.  parent[i] must be -1 or an earlier node; the walk stops at the
+// first parent that is not, and flags BAD_PARENT.  At most T steps because
+// every accepted parent is strictly smaller than its child.
+__device__ __forceinline__ uint64_t ancestor_bits(const int32_t* parent, int i, int T,
+                                                  uint32_t* status) {
+  uint64_t bits = 0;
+  int a = i;
+  for (int step = 0; step < T && a >= 0; ++step) {
+    bits |= 1ull << a;
+    int p = __ldg(parent + a);
+    if (p < -1 || p >= a) {
+      if (status) atomicOr(status, DDTREE_ST_BAD_PARENT);
+      break;
+    }
+    a = p;
+  }
+  return bits;
+}
+
+__device__ __forceinline__ float bf16_lo(uint32_t v) { return __uint_as_float(v << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t v) { return __uint_as_float(v & 0xffff0000u); }
+
+// ---- launchers (one per .cu file) ----
+cudaError_t launch_partial_simt(const VerifyArgs& a, cudaStream_t stream);
+cudaError_t launch_partial_tc(const VerifyArgs& a, cudaStream_t stream);
+cudaError_t launch_combine(const VerifyArgs& a, cudaStream_t stream);
+cudaError_t launch_ancestor_mask(const int32_t* parent, int batch, int n_nodes, uint64_t* anc,
+                                 uint32_t* status, cudaStream_t stream);
+
+}  // namespace ddtree

@@ -1,0 +1,130 @@
+"""C-ABI checks that need no GPU: the library loads, exports every entry
+point include/ddtree_verify.h declares, plans deterministically, and rejects
+bad arguments on the host before touching a device."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from speculative_decode_tree_gb300 import binding as B
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _declared():
+    names = []
+    for fn in os.listdir(os.path.join(ROOT, "include")):
+        if fn.endswith(".h"):
+            text = open(os.path.join(ROOT, "include", fn)).read()
+            names += re.findall(r"DDTREE_API\s+[\w\s\*]+?\b(ddtree_\w+)\s*\(", text)
+    return sorted(set(names))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from speculative_decode_tree_gb300.build import build
+    build()
+    return B.library()
+
+
+def test_every_declared_symbol_is_exported(lib):
+    declared = _declared()
+    assert len(declared) >= 8
+    for name in declared:
+        assert hasattr(lib, name), name
+    assert set(B.EXPORTS) <= set(declared)
+
+
+def test_status_strings(lib):
+    for code in range(0, 7):
+        assert B.ddtree_status_str(code)
+    assert B.ddtree_status_str(99) == "unknown status"
+
+
+def test_plan_fills_the_sms_and_sizes_the_workspace(lib):
+    p = B.ddtree_verify_mla_plan_ex(1, 32, 8, [65536], 262144, 148, B.DDTREE_KERNEL_SIMT)
+    assert p.rows_per_req == 256 and p.row_tile == 32 and p.row_tiles == 8
+    assert p.chunk_keys % p.tile_keys == 0
+    items = p.row_tiles * p.total_splits
+    assert items >= 4 * 148 * 0.9
+    assert p.total_splits == -(-(65536 + 32) // p.chunk_keys)
+    ws = B.ddtree_verify_mla_workspace_size(p)
+    assert ws == p.workspace_bytes and ws % 256 == 0
+    assert ws >= 256 + p.total_splits * 256 * (512 + 1) * 4
+    # Deterministic.
+    q = B.ddtree_verify_mla_plan_ex(1, 32, 8, [65536], 262144, 148, B.DDTREE_KERNEL_SIMT)
+    assert p.as_dict() == q.as_dict()
+
+
+def test_plan_batch_splits_sum_per_request(lib):
+    prefixes = [1024, 4096, 8192, 16384, 32768, 65536, 131072, 189440]
+    p = B.ddtree_verify_mla_plan_ex(8, 32, 8, prefixes, 524288, 148, B.DDTREE_KERNEL_SIMT)
+    assert p.total_splits == sum(-(-(P + 32) // p.chunk_keys) for P in prefixes)
+    assert p.max_keys == 189440 + 32
+
+
+@pytest.mark.parametrize("args", [
+    (0, 4, 8), (1, 0, 8), (1, 65, 8), (1, 4, 0), (1, 4, 129), (1025, 4, 8),
+])
+def test_plan_rejects_bad_sizes(lib, args):
+    b, t, h = args
+    with pytest.raises(B.DDTreeError) as e:
+        B.ddtree_verify_mla_plan_ex(b, t, h, [16] * max(b, 1), 1024, 148)
+    assert e.value.code == B.DDTREE_EINVAL
+
+
+def test_plan_rejects_negative_prefix(lib):
+    with pytest.raises(B.DDTreeError):
+        B.ddtree_verify_mla_plan_ex(2, 4, 8, [16, -1], 1024, 148)
+
+
+def test_null_pointers_rejected_before_device_use(lib):
+    p = B.ddtree_verify_mla_plan_ex(1, 4, 8, [256], 1024, 148)
+    rc = lib.ddtree_verify_mla_batched(ctypes.byref(p), None, None, None, None, None, None, None,
+                                       0.1, None, None, None, 0, None)
+    assert rc == B.DDTREE_EINVAL
+
+
+def test_tampered_plan_rejected(lib):
+    p = B.ddtree_verify_mla_plan_ex(1, 4, 8, [256], 1024, 148)
+    p.workspace_bytes -= 256
+    fake = ctypes.c_void_p(256)  # never dereferenced: validation fails first
+    rc = lib.ddtree_verify_mla_batched(ctypes.byref(p), fake, fake, fake, fake, fake, fake, fake,
+                                       0.1, fake, fake, fake, 1 << 20, None)
+    assert rc == B.DDTREE_EINVAL
+
+
+def test_misaligned_pointer_rejected(lib):
+    p = B.ddtree_verify_mla_plan_ex(1, 4, 8, [256], 1024, 148)
+    ok = ctypes.c_void_p(1 << 12)
+    bad = ctypes.c_void_p((1 << 12) + 8)
+    rc = lib.ddtree_verify_mla_batched(ctypes.byref(p), bad, ok, ok, ok, ok, ok, ok,
+                                       0.1, ok, ok, ok, 1 << 30, None)
+    assert rc == B.DDTREE_EINVAL
+
+
+def test_small_workspace_rejected(lib):
+    p = B.ddtree_verify_mla_plan_ex(1, 4, 8, [256], 1024, 148)
+    ok = ctypes.c_void_p(1 << 12)
+    rc = lib.ddtree_verify_mla_batched(ctypes.byref(p), ok, ok, ok, ok, ok, ok, ok,
+                                       0.1, ok, ok, ok, p.workspace_bytes - 1, None)
+    assert rc == B.DDTREE_EWORKSPACE
+
+
+def test_nonfinite_scale_rejected(lib):
+    p = B.ddtree_verify_mla_plan_ex(1, 4, 8, [256], 1024, 148)
+    ok = ctypes.c_void_p(1 << 12)
+    rc = lib.ddtree_verify_mla_batched(ctypes.byref(p), ok, ok, ok, ok, ok, ok, ok,
+                                       float("nan"), ok, ok, ok, 1 << 30, None)
+    assert rc == B.DDTREE_EINVAL
+
+
+def test_no_device_reports_unsupported(lib):
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a device is present")
+    p = B.Plan()
+    arr = (ctypes.c_int32 * 1)(256)
+    rc = lib.ddtree_verify_mla_plan(1, 4, 8, ctypes.cast(arr, ctypes.c_void_p), 1024, ctypes.byref(p))
+    assert rc == B.DDTREE_EUNSUPPORTED

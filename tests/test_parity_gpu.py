@@ -1,0 +1,243 @@
+"""GPU parity: the CUDA path through the C ABI against the float64 oracle on
+the same seeded inputs, element by element.  Small shapes compare every
+row; the five full-size workloads compare every row where the oracle is
+quick and sampled rows elsewhere, in the launch configuration the
+benchmark times (the plan the library picks)."""
+import pytest
+import torch
+
+from oracle import ancestor_bits
+from speculative_decode_tree_gb300 import binding as B
+from speculative_decode_tree_gb300.runner import DeviceVerify
+from speculative_decode_tree_gb300.workloads import make_inputs
+from parity_util import assert_within_tolerance, cached_workload, oracle_rows
+
+pytestmark = pytest.mark.gpu
+
+KERNELS = [B.DDTREE_KERNEL_SIMT]
+
+
+def _compare_all(inp, kernel=None, what=""):
+    dv = DeviceVerify(inp, kernel=kernel)
+    dv.run()
+    torch.cuda.synchronize()
+    assert dv.status() == 0
+    T, H = inp.n_nodes, inp.n_heads
+    for b in range(inp.batch):
+        O_ref, L_ref = oracle_rows(inp, b)
+        assert_within_tolerance(dv.out[b * T:(b + 1) * T], dv.lse[b * T:(b + 1) * T], O_ref, L_ref,
+                                f"{what} request {b}")
+    return dv
+
+
+SMALL = [
+    # (P, T, H, tree, batch)
+    (256, 4, 8, "chain", 1),
+    (0, 1, 1, "chain", 1),
+    (1, 1, 8, "chain", 1),
+    (0, 5, 2, "uniform", 1),
+    (37, 16, 8, "uniform", 1),
+    (1000, 32, 8, "uniform", 1),
+    (4097, 16, 8, "uniform", 1),
+    (300, 64, 2, "bounded", 1),
+    (129, 3, 128, "uniform", 1),
+    (2000, 8, 16, "uniform", 1),
+]
+
+
+@pytest.mark.parametrize("kernel", KERNELS)
+@pytest.mark.parametrize("shape", SMALL, ids=[f"P{s[0]}_T{s[1]}_H{s[2]}_{s[3]}" for s in SMALL])
+def test_small_shapes_match_oracle(shape, kernel):
+    P, T, H, tree, batch = shape
+    inp = make_inputs("small", batch=batch, n_heads=H, prefixes=[P] * batch, n_nodes=T, tree=tree,
+                      pool_rows=max(1024, 2 * (P + T)), index_mode="sample", seed=P + 7 * T + H)
+    _compare_all(inp, kernel, f"P={P} T={T} H={H}")
+
+
+@pytest.mark.parametrize("kernel", KERNELS)
+def test_ragged_batch_matches_oracle(kernel):
+    prefixes = [0, 5, 777, 64, 1, 2049, 31, 300]
+    inp = make_inputs("ragged", batch=8, n_heads=4, prefixes=prefixes, n_nodes=12, tree="uniform",
+                      pool_rows=8192, index_mode="interleaved", seed=41)
+    _compare_all(inp, kernel, "ragged batch")
+
+
+@pytest.mark.parametrize("kernel", KERNELS)
+@pytest.mark.parametrize("P", [0, 16, 256, 4096])
+def test_spiked_tree_keys_make_the_mask_visible(P, kernel):
+    """Tree keys score ~70 nats above prefix keys, so each node's output is
+    the mean of V over its ancestors: a wrong mask moves O far past tolerance."""
+    T, H = 16, 8
+    inp = make_inputs("spiked", batch=1, n_heads=H, prefixes=[P], n_nodes=T, tree="uniform",
+                      pool_rows=max(1024, 2 * (P + T)), index_mode="sample", seed=53 + P)
+    inp.q_latent.zero_()
+    inp.q_rope.zero_()
+    inp.q_rope[..., 0] = 8.0
+    inp.kv_pool[inp.kv_indices[P:].long(), 512] = 128.0
+    dv = _compare_all(inp, kernel, f"spiked P={P}")
+    # The mask is visible: dropping one node's deepest ancestor changes O by >= 0.1.
+    O_ref, _ = oracle_rows(inp, 0)
+    par = inp.tree_parent[0].tolist()
+    for i in range(T):
+        if par[i] >= 0:
+            wrong = list(par)
+            wrong[i] = -1
+            inp2 = make_inputs("spiked", batch=1, n_heads=H, prefixes=[P], n_nodes=T, tree="uniform",
+                               pool_rows=max(1024, 2 * (P + T)), index_mode="sample", seed=53 + P)
+            inp2.kv_pool = inp.kv_pool
+            inp2.q_latent, inp2.q_rope = inp.q_latent, inp.q_rope
+            inp2.tree_parent = torch.tensor([wrong], dtype=torch.int32)
+            O_wrong, _ = oracle_rows(inp2, 0)
+            assert float((O_wrong[i] - O_ref[i]).abs().max()) >= 0.1
+            assert float((dv.out[i].double().cpu() - O_wrong[i]).abs().max()) >= 0.09
+            break
+
+
+@pytest.mark.parametrize("name", ["tiny", "tp8_slice", "long_scattered"])
+def test_full_workload_all_rows(name):
+    inp = cached_workload(name)
+    _compare_all(inp, None, name)
+
+
+def test_long_contiguous_equals_scattered_bitwise():
+    a = DeviceVerify(cached_workload("long_scattered"))
+    a.run()
+    b = DeviceVerify(cached_workload("long_contiguous"))
+    b.run()
+    torch.cuda.synchronize()
+    assert torch.equal(a.out, b.out) and torch.equal(a.lse, b.lse)
+    inp = cached_workload("long_contiguous")
+    O_ref, L_ref = oracle_rows(inp, 0, nodes=[0, 31])
+    assert_within_tolerance(b.out[[0, 31]], b.lse[[0, 31]], O_ref, L_ref, "long_contiguous")
+
+
+def test_unsharded_heads_sampled_rows():
+    inp = cached_workload("unsharded_heads")
+    dv = DeviceVerify(inp)
+    dv.run()
+    torch.cuda.synchronize()
+    assert dv.status() == 0
+    par = inp.tree_parent[0].tolist()
+    depth = []
+    for i, p in enumerate(par):
+        depth.append(1 if p < 0 else depth[p] + 1)
+    deepest = max(range(len(par)), key=lambda i: depth[i])
+    nodes = sorted({0, 1, 31, 63, deepest})
+    O_ref, L_ref = oracle_rows(inp, 0, nodes=nodes)
+    assert_within_tolerance(dv.out[nodes], dv.lse[nodes], O_ref, L_ref, "unsharded_heads")
+
+
+def test_mixed_batch_sampled_rows():
+    inp = cached_workload("mixed_batch")
+    dv = DeviceVerify(inp)
+    dv.run()
+    torch.cuda.synchronize()
+    assert dv.status() == 0
+    T = inp.n_nodes
+    for b in range(inp.batch):
+        nodes = [0, 17, 31]
+        O_ref, L_ref = oracle_rows(inp, b, nodes=nodes)
+        rows = [b * T + n for n in nodes]
+        assert_within_tolerance(dv.out[rows], dv.lse[rows], O_ref, L_ref, f"mixed request {b}")
+
+
+def test_single_request_entry_point_matches_batched():
+    inp = make_inputs("single", batch=1, n_heads=8, prefixes=[3000], n_nodes=16, tree="uniform",
+                      pool_rows=8192, index_mode="sample", seed=61)
+    dv = DeviceVerify(inp, check_pool=False)
+    dv.run()
+    o1, l1 = dv.out.clone(), dv.lse.clone()
+    dv.out.zero_()
+    dv.run_single()
+    torch.cuda.synchronize()
+    assert torch.equal(o1, dv.out) and torch.equal(l1, dv.lse)
+
+
+def test_ancestor_mask_stage_bit_exact():
+    g = torch.Generator().manual_seed(71)
+    B_, T = 5, 64
+    par = []
+    for b in range(B_):
+        par.append([int(torch.randint(-1, i, (1,), generator=g)) for i in range(T)])
+    parent = torch.tensor(par, dtype=torch.int32, device="cuda")
+    anc = torch.empty(B_ * T, dtype=torch.int64, device="cuda")
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    B.ddtree_build_ancestor_mask(parent, B_, T, anc, status)
+    torch.cuda.synchronize()
+    got = [v & ((1 << 64) - 1) for v in anc.tolist()]
+    want = sum((ancestor_bits(p) for p in par), [])
+    assert got == want and int(status) == 0
+    parent[1, 7] = 9  # not an earlier node
+    B.ddtree_build_ancestor_mask(parent, B_, T, anc, status)
+    torch.cuda.synchronize()
+    assert int(status) & B.DDTREE_ST_BAD_PARENT
+
+
+def test_bad_device_data_is_flagged_not_dereferenced():
+    inp = make_inputs("bad", batch=1, n_heads=8, prefixes=[500], n_nodes=8, tree="uniform",
+                      pool_rows=2048, index_mode="sample", seed=73)
+    dv = DeviceVerify(inp)
+    dv.kv_indices[3] = inp.pool_rows + 1000
+    dv.kv_indices[4] = -5
+    dv.run()
+    torch.cuda.synchronize()
+    assert dv.status() & B.DDTREE_ST_BAD_INDEX
+    assert torch.isfinite(dv.out.float()).all()
+    dv2 = DeviceVerify(inp)
+    dv2.tree_parent[0, 5] = 6
+    dv2.run()
+    torch.cuda.synchronize()
+    assert dv2.status() & B.DDTREE_ST_BAD_PARENT
+    dv3 = DeviceVerify(inp)
+    dv3.prefix_lens[0] = 500 + dv3.plan.chunk_keys * 3  # longer than planned
+    dv3.kv_indptr[1] = 500 + dv3.plan.chunk_keys * 3 + 8
+    dv3.run()
+    torch.cuda.synchronize()
+    assert dv3.status() & B.DDTREE_ST_BAD_LENGTH
+
+
+def test_graph_capture_and_replay_with_new_inputs_and_shorter_prefix():
+    P, T, H = 6000, 16, 8
+    inp = make_inputs("graph", batch=1, n_heads=H, prefixes=[P], n_nodes=T, tree="uniform",
+                      pool_rows=16384, index_mode="sample", seed=79)
+    dv = DeviceVerify(inp)
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        dv.run()  # warm-up (sets kernel attributes) outside capture
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        dv.run()
+    # New queries and indices, same shapes.
+    inp2 = make_inputs("graph", batch=1, n_heads=H, prefixes=[P], n_nodes=T, tree="uniform",
+                       pool_rows=16384, index_mode="sample", seed=83)
+    inp2.kv_pool = inp.kv_pool
+    dv.q_latent.copy_(inp2.q_latent)
+    dv.q_rope.copy_(inp2.q_rope)
+    dv.kv_indices.copy_(inp2.kv_indices)
+    dv.tree_parent.copy_(inp2.tree_parent)
+    g.replay()
+    torch.cuda.synchronize()
+    O_ref, L_ref = oracle_rows(inp2, 0)
+    assert_within_tolerance(dv.out, dv.lse, O_ref, L_ref, "graph replay")
+    eager = DeviceVerify(inp2)
+    eager.run()
+    torch.cuda.synchronize()
+    assert torch.equal(eager.out, dv.out) and torch.equal(eager.lse, dv.lse)
+    # Shorter prefix on replay: lengths are read on the device.
+    P2 = 2500
+    idx_short = torch.cat([inp2.kv_indices[:P2], inp2.kv_indices[P:]])
+    dv.kv_indices[:P2 + T].copy_(idx_short)
+    dv.prefix_lens.fill_(P2)
+    dv.kv_indptr[1] = P2 + T
+    g.replay()
+    torch.cuda.synchronize()
+    assert dv.status() == 0
+    inp3 = make_inputs("graph", batch=1, n_heads=H, prefixes=[P2], n_nodes=T, tree="uniform",
+                       pool_rows=16384, index_mode="sample", seed=83)
+    inp3.kv_pool, inp3.q_latent, inp3.q_rope = inp.kv_pool, inp2.q_latent, inp2.q_rope
+    inp3.kv_indices, inp3.tree_parent = idx_short.to(torch.int32), inp2.tree_parent
+    O_ref3, L_ref3 = oracle_rows(inp3, 0)
+    assert_within_tolerance(dv.out, dv.lse, O_ref3, L_ref3, "graph replay, shorter prefix")
