@@ -220,6 +220,41 @@ DDTREE_API int ddtree_build_ancestor_mask(const int32_t* tree_parent, int batch,
 DDTREE_API int ddtree_verify_mla_check(const void* workspace, struct CUstream_st* stream,
                             uint32_t* host_status);
 
+/*
+ * Single-request verify attention that allocates nothing and needs no
+ * workspace.  The pages have no counterpart of this entry point; it is an
+ * addition for callers that cannot allocate device memory where they call
+ * verify attention (an allocator that forbids raw cudaMalloc, a code path
+ * where an allocation would synchronise the device, or a host integration
+ * with nowhere to keep a workspace buffer).
+ *
+ * Arguments, layouts and results are those of ddtree_verify_mla without the
+ * workspace.  The split-KV partials go to a scratch array built into the
+ * library: DDTREE_NOALLOC_SCRATCH_BYTES (32 MiB) of device memory that every
+ * GPU loading the library keeps until the process exits.  When the usual
+ * plan would need more scratch than that, the call uses fewer, longer KV
+ * splits; a shape that does not fit even with one split per request returns
+ * DDTREE_EWORKSPACE (with the current limits of 64 nodes x 128 heads every
+ * accepted shape fits).
+ *  - The first call on each device looks up the scratch array's device
+ *    address (cudaGetSymbolAddress, which can load the module); make that
+ *    first call before any stream capture.
+ *  - All calls on a device share the one scratch array, which keeps the
+ *    previous call's contents; each call clears the status word it uses and
+ *    writes every partial it reads.  Calls whose GPU work overlaps (other
+ *    streams, other host threads) race on the array: serialise them.
+ *  - The status word lives in the library's scratch, so device-data errors
+ *    are not observable through this entry point; indices are not checked
+ *    against the pool size (as in ddtree_verify_mla).
+ *  - Calls no cudaMalloc, cudaFree or allocating library routine.
+ */
+#define DDTREE_NOALLOC_SCRATCH_BYTES (32u << 20)
+DDTREE_API int ddtree_verify_mla_noalloc(const ddtree_bf16_t* q_latent, const ddtree_bf16_t* q_rope,
+                              const ddtree_bf16_t* kv_pool, const int32_t* kv_indices,
+                              int prefix_len, const int32_t* tree_parent,
+                              int n_nodes, int n_heads, float sm_scale,
+                              ddtree_bf16_t* out, float* lse, struct CUstream_st* stream);
+
 /* Static text for a DDTREE_* return code. */
 DDTREE_API const char* ddtree_status_str(int code);
 

@@ -37,6 +37,7 @@ EXPORTS = (
     "ddtree_verify_mla_plan", "ddtree_verify_mla_plan_ex", "ddtree_verify_mla_workspace_size",
     "ddtree_verify_mla", "ddtree_verify_mla_batched", "ddtree_build_ancestor_mask",
     "ddtree_verify_mla_check", "ddtree_status_str", "ddtree_verify_mla_batched_timed",
+    "ddtree_verify_mla_noalloc",
 )
 
 
@@ -85,12 +86,13 @@ def library() -> ctypes.CDLL:
     L.ddtree_verify_mla_batched_timed.argtypes = [P, vp, vp, vp, vp, vp, vp, vp, f32, vp, vp, vp, sz,
                                                   vp, vp]
     L.ddtree_build_ancestor_mask.argtypes = [vp, i32, i32, vp, vp, vp]
+    L.ddtree_verify_mla_noalloc.argtypes = [vp, vp, vp, vp, i32, vp, i32, i32, f32, vp, vp, vp]
     L.ddtree_verify_mla_check.argtypes = [vp, vp, ctypes.POINTER(ctypes.c_uint32)]
     L.ddtree_status_str.argtypes = [i32]
     L.ddtree_status_str.restype = ctypes.c_char_p
     for name in ("ddtree_verify_mla_plan", "ddtree_verify_mla_plan_ex", "ddtree_verify_mla",
                  "ddtree_verify_mla_batched", "ddtree_build_ancestor_mask", "ddtree_verify_mla_check",
-                 "ddtree_verify_mla_batched_timed"):
+                 "ddtree_verify_mla_batched_timed", "ddtree_verify_mla_noalloc"):
         getattr(L, name).restype = i32
     _lib = L
     return L
@@ -156,6 +158,20 @@ def ddtree_verify_mla(q_latent, q_rope, kv_pool, kv_indices, prefix_len: int, tr
         int(n_nodes), int(n_heads), float(sm_scale), _dev(out, bf, "out"),
         _dev(lse, torch.float32, "lse"), _dev(workspace, torch.uint8, "workspace"), _stream(stream))
     _check(rc, "ddtree_verify_mla")
+
+
+def ddtree_verify_mla_noalloc(q_latent, q_rope, kv_pool, kv_indices, prefix_len: int, tree_parent,
+                              n_nodes: int, n_heads: int, sm_scale: float, out, lse,
+                              stream=None) -> None:
+    """ddtree_verify_mla without a workspace: for callers that cannot allocate
+    device memory; the partials use the library's built-in scratch array."""
+    bf, i32 = torch.bfloat16, torch.int32
+    rc = library().ddtree_verify_mla_noalloc(
+        _dev(q_latent, bf, "q_latent"), _dev(q_rope, bf, "q_rope"), _dev(kv_pool, bf, "kv_pool"),
+        _dev(kv_indices, i32, "kv_indices"), int(prefix_len), _dev(tree_parent, i32, "tree_parent"),
+        int(n_nodes), int(n_heads), float(sm_scale), _dev(out, bf, "out"),
+        _dev(lse, torch.float32, "lse"), _stream(stream))
+    _check(rc, "ddtree_verify_mla_noalloc")
 
 
 def ddtree_verify_mla_batched(plan: Plan, q_latent, q_rope, kv_pool, kv_indices, kv_indptr,
