@@ -63,15 +63,15 @@ struct Geometry {
   int row_tile, tile_keys, waves;
 };
 Geometry geometry(int kernel) {
-  if (kernel == DDTREE_KERNEL_TC) return Geometry{128, 64, 1};
+  if (kernel == DDTREE_KERNEL_TC) return Geometry{128, 128, 1};
   return Geometry{32, 32, 4};
 }
 
+// The tensor-core kernel works on 128-row tiles of 128 keys; below about one
+// such tile's worth of (row, key) pairs the CUDA-core kernel is used.
 int choose_kernel(int kernel, int rows_per_req, int64_t total_keys) {
   if (kernel != DDTREE_KERNEL_AUTO) return kernel;
-  (void)rows_per_req;
-  (void)total_keys;
-  return DDTREE_KERNEL_SIMT;
+  return ((int64_t)rows_per_req * total_keys >= 128 * 1024) ? DDTREE_KERNEL_TC : DDTREE_KERNEL_SIMT;
 }
 
 }  // namespace
@@ -113,8 +113,9 @@ extern "C" int ddtree_verify_mla_plan_ex(int batch, int n_nodes, int n_heads,
   p.row_tiles = (p.rows_per_req + g.row_tile - 1) / g.row_tile;
 
   // Split rule: enough work items (row tile x key chunk) for `waves` CTAs
-  // per SM, with chunks a whole number of tiles.
-  int64_t target_items = (int64_t)g.waves * num_sms;
+  // per SM, with chunks a whole number of tiles.  A tensor-core work item is
+  // a cluster of two CTAs (scorer + accumulator), so it occupies two SMs.
+  int64_t target_items = (int64_t)g.waves * num_sms / (p.kernel == DDTREE_KERNEL_TC ? 2 : 1);
   int64_t target_splits = std::max<int64_t>(1, (target_items + p.row_tiles - 1) / p.row_tiles);
   int64_t chunk = (total_keys + target_splits - 1) / target_splits;
   chunk = round_up(std::max<int64_t>(chunk, g.tile_keys), g.tile_keys);

@@ -1,7 +1,579 @@
-// Tensor-core (tcgen05 / TMEM) split-KV partial stage — placeholder until the
-// kernel lands; plans never select it yet.
+// Split-KV partial stage on the tcgen05 tensor cores (sm_103a).
+//
+// One work item = 128 query rows (node-major (node, head) rows of one request)
+// x one chunk of that request's key sequence, run by a cluster of two CTAs
+// with different jobs ("Chunk 66.0": KV-split flash decode, partial + reduce;
+// the split count is the plan's, "Chunk 66.1"):
+//
+//  scorer (cluster rank 0)
+//    Q latent (128 x 512 bf16) lives in TMEM as the A operand, Q rope in
+//    shared memory; per tile of 128 keys it gathers the 576-wide key rows
+//    through the page_size=1 index table with 16-byte cp.async into
+//    128-byte-swizzled chunks of 64 columns ("Chunk 66.1": 128-bit loads),
+//    issues S = Q K^T (M=128, N=128, K=576) into one of two TMEM S buffers,
+//    and four softmax warps (one query row per thread) apply the ancestor
+//    mask on tree keys only, keep a running max with lazy rescaling, and
+//    write P = exp(s - m) as a bf16 K-major tile plus per-row rescale
+//    factors, which one thread ships to the peer with a bulk shared-memory
+//    copy across the cluster.
+//  accumulator (cluster rank 1)
+//    holds O (128 x 512 fp32) in all 512 TMEM columns, gathers the value
+//    rows (first 512 columns of the same keys) as MN-major operands, and
+//    issues O += P V (M=128, N=128 per quarter, K=128 keys) from the P tiles
+//    it receives.  Its epilogue warps rescale O rows when the scorer's
+//    running max moved (rare), and at the end write O_s = O / l.
+//
+// Work per (row, key): 576 MACs on the scorer, 512 on the accumulator.
+// Every mbarrier wait is bounded; on expiry the kernel sets
+// DDTREE_ST_TIMEOUT, stops issuing work, waits (bounded) for its own
+// tensor-core work and frees its TMEM.
 #include "common.cuh"
+#include "tc_ptx.cuh"
 
 namespace ddtree {
-cudaError_t launch_partial_tc(const VerifyArgs&, cudaStream_t) { return cudaErrorNotSupported; }
+namespace {
+
+using namespace ptx;
+
+constexpr int TK = 128;                 // keys per tile
+constexpr int ROWS = 128;               // query rows per work item
+constexpr int CHUNK = 16384;            // one 64-column chunk of a tile: 128 keys x 128 B
+constexpr int QRING = 8;                // scorer key-chunk slots
+constexpr int VRING = 4;                // accumulator slots, each a pair of chunks (32 KB)
+constexpr int PTILE = 32768;            // bf16 P tile: 2 swizzle atoms of 128 rows x 128 B
+constexpr int META = 1040;              // alpha[128], lfin[128], flag words[4]
+constexpr int PCOPY = PTILE + META;     // bytes shipped per tile (multiple of 16)
+constexpr int PBUF = 34816;             // P buffer stride (1024-aligned)
+constexpr int kThreads = 256;
+constexpr float kLazyRescale = 8.0f;    // rescale only when the max grows by > 2^8 (log2 units)
+constexpr uint64_t kWaitNs = 2000000000ull;
+
+// Shared-memory map (offsets from a 1024-aligned base).
+constexpr int Q_ROPE = 0;                               // scorer: 16 KB
+constexpr int Q_RING = Q_ROPE + CHUNK;                  // scorer: 8 x 16 KB
+constexpr int Q_STAGE = Q_RING + QRING * CHUNK;         // scorer: 2 x PBUF
+constexpr int Q_END = Q_STAGE + 2 * PBUF;
+constexpr int V_PBUF = 0;                               // accumulator: 2 x PBUF
+constexpr int V_RING = V_PBUF + 2 * PBUF;               // accumulator: 4 x 32 KB
+constexpr int V_END = V_RING + VRING * 2 * CHUNK;
+constexpr int BIG_END = (Q_END > V_END ? Q_END : V_END);
+
+struct __align__(8) Ctrl {
+  uint64_t kfull[QRING], kempty[QRING];  // scorer ring
+  uint64_t sfull[2], sempty[2];          // scorer S buffers
+  uint64_t pfree[2];                     // scorer: peer released P buffer (2 arrivals)
+  uint64_t vfull[VRING], vempty[VRING];  // accumulator ring
+  uint64_t pfull[2];                     // accumulator: P tile landed (tx)
+  uint64_t pvdone[2];                    // accumulator: PV of a tile finished
+  uint64_t corr_done;                    // accumulator: O rows rescaled
+  uint64_t mma_done;                     // last tensor-core work of this CTA finished
+  uint32_t tmem_base;
+  uint32_t abort;
+  uint32_t key_mask[2][4];               // scorer: valid-key bits per tile parity
+  uint64_t anc[64];                      // scorer: ancestor bits per node
+};
+
+constexpr size_t kSmemBytes = 1024 + BIG_END + sizeof(Ctrl) + 64;
+
+__device__ __forceinline__ void set_abort(Ctrl* c, uint32_t* status) {
+  c->abort = 1;
+  atomicOr(status, DDTREE_ST_TIMEOUT);
+}
+
+// Bounded wait; on expiry mark the CTA aborted.  Returns false when aborted.
+__device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, Ctrl* c, uint32_t* status) {
+  if (*(volatile uint32_t*)&c->abort) return false;
+  if (mbar_wait(bar, parity, global_timer_ns() + kWaitNs)) return true;
+  set_abort(c, status);
+  return false;
+}
+__device__ __forceinline__ bool wait_cluster_or_abort(uint64_t* bar, uint32_t parity, Ctrl* c,
+                                                      uint32_t* status) {
+  if (*(volatile uint32_t*)&c->abort) return false;
+  if (mbar_wait_cluster(bar, parity, global_timer_ns() + kWaitNs)) return true;
+  set_abort(c, status);
+  return false;
+}
+
+__device__ __forceinline__ void named_bar(int id, int nthreads) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
+// Named barrier that also ORs a predicate over the participating threads,
+// so every thread takes the same decision (used to stop after an abort).
+__device__ __forceinline__ bool named_bar_or(int id, int nthreads, bool pred) {
+  uint32_t out;
+  asm volatile(
+      "{ .reg .pred p, q; setp.ne.u32 p, %1, 0;\n"
+      "  bar.red.or.pred q, %2, %3, p;\n"
+      "  selp.u32 %0, 1, 0, q; }"
+      : "=r"(out)
+      : "r"((uint32_t)pred), "r"(id), "r"(nthreads)
+      : "memory");
+  return out != 0;
+}
+__device__ __forceinline__ bool aborted(Ctrl* c) { return *(volatile uint32_t*)&c->abort != 0; }
+
+// Gathers `nchunks` consecutive 64-column chunks (starting at column chunk
+// c0) of the tile's 128 key rows into `dst` (chunk stride CHUNK), 128-byte
+// swizzled, then arrives on `bar` when the copies land.  Lane l handles key
+// rows (l >> 3) + 4 i and 16-byte piece (l & 7) of each 128-byte chunk row.
+__device__ __forceinline__ void gather_chunks(uint8_t* dst, const uint16_t* pool, const int32_t (&idx)[32],
+                                              int c0, int nchunks, int lane, uint64_t* bar) {
+  const int piece = lane & 7;
+  for (int c = 0; c < nchunks; ++c) {
+    const uint32_t base = smem_u32(dst + c * CHUNK);
+#pragma unroll 8
+    for (int i = 0; i < 32; ++i) {
+      const int key = (lane >> 3) + 4 * i;
+      const int id = idx[i];
+      const uint32_t d = base + key * 128 + ((piece ^ (key & 7)) << 4);
+      const uint16_t* src = pool + (size_t)(id < 0 ? 0 : id) * kRow + (c0 + c) * 64 + piece * 8;
+      cp_async16_zfill(d, src, id < 0 ? 0u : 16u);
+    }
+  }
+  cp_async_mbar_arrive(bar);
+}
+
+struct Item {
+  SplitLoc loc;
+  int row0;      // first query row of the tile within the request
+  int k_begin;   // first key of the chunk
+  int k_end;     // one past the last key
+  int ntiles;
+  int slot;      // split slot in the workspace
+};
+
+// Loads the tile's 128 indices for this lane (keys (lane>>3) + 4i); -1 for
+// keys past the chunk end or outside the pool (the latter flagged).
+__device__ __forceinline__ void load_tile_indices(const VerifyArgs& a, const Item& it, int tile, int lane,
+                                                  int32_t (&idx)[32]) {
+  const int k0 = it.k_begin + tile * TK;
+#pragma unroll
+  for (int i = 0; i < 32; ++i) {
+    const int kp = k0 + (lane >> 3) + 4 * i;
+    int id = -1;
+    if (kp < it.k_end) {
+      id = __ldg(a.kv_indices + it.loc.idx_base + kp);
+      if (id < 0 || (a.pool_rows > 0 && id >= a.pool_rows)) id = -1;
+    }
+    idx[i] = id;
+  }
+}
+
+// ------------------------------------------------------------------ scorer
+__device__ void scorer(const VerifyArgs& a, const Item& it, uint8_t* sm, Ctrl* c) {
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const uint32_t tmem = c->tmem_base;        // cols [0,256): Q latent; [256,384), [384,512): S
+  const uint32_t peer = 1;
+
+  if (warp == 0) {
+    // ---- producer: key chunks 0..8 of every tile
+    int32_t idx[32];
+    int n = 0;
+    for (int t = 0; t < it.ntiles; ++t) {
+      load_tile_indices(a, it, t, lane, idx);
+      for (int ch = 0; ch < 9; ++ch, ++n) {
+        const int slot = n % QRING;
+        if (!wait_or_abort(&c->kempty[slot], ((n / QRING) & 1) ^ 1, c, a.status)) {
+          asm volatile("cp.async.wait_all;" ::: "memory");
+          return;
+        }
+        gather_chunks(sm + Q_RING + slot * CHUNK, a.kv_pool, idx, ch, 1, lane, &c->kfull[slot]);
+      }
+    }
+  } else if (warp == 1) {
+    // ---- MMA issuer (one thread)
+    if (lane == 0) {
+      constexpr uint32_t idesc = idesc_bf16_f32(128, 128, false, false);
+      const uint64_t rope_desc = desc_sw128(smem_u32(sm + Q_ROPE), 16, 1024);
+      int n = 0;
+      bool ok = true;
+      for (int t = 0; t < it.ntiles && ok; ++t) {
+        const int s = t & 1;
+        const uint32_t sbuf = tmem + 256 + 128 * s;
+        if (!wait_or_abort(&c->sempty[s], ((t >> 1) & 1) ^ 1, c, a.status)) { ok = false; break; }
+        tc_fence_after();
+        for (int ch = 0; ch < 9; ++ch, ++n) {
+          const int slot = n % QRING;
+          if (!wait_or_abort(&c->kfull[slot], (n / QRING) & 1, c, a.status)) { ok = false; break; }
+          fence_async_smem();  // cp.async (generic proxy) data -> tensor-core reads
+          tc_fence_after();
+          const uint64_t kdesc = desc_sw128(smem_u32(sm + Q_RING + slot * CHUNK), 16, 1024);
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk) {
+            const int ks = ch * 4 + kk;
+            const uint64_t bd = kdesc + (uint64_t)((kk * 32) >> 4);
+            if (ch < 8) mma_ts(sbuf, tmem + ks * 8, bd, idesc, ks > 0);
+            else mma_ss(sbuf, rope_desc + (uint64_t)((kk * 32) >> 4), bd, idesc, 1);
+          }
+          mma_commit(&c->kempty[slot]);
+        }
+        if (ok) mma_commit(&c->sfull[s]);
+      }
+      mma_commit(&c->mma_done);
+    }
+  } else if (warp >= 4) {
+    // ---- softmax: thread = query row r
+    const int r = tid - 128;
+    const int w = warp - 4;
+    const int req_row = it.row0 + r;
+    const bool row_ok = req_row < a.rows_per_req;
+    const uint64_t anc = row_ok ? c->anc[req_row / a.n_heads] : 0ull;
+    const float scale2 = a.sm_scale * 1.4426950408889634f;  // scores in log2 units
+    float m_ref = -INFINITY, l = 0.f;
+    const uint32_t my_lane_addr = (uint32_t)(w * 32) << 16;
+    const uint32_t peer_pbuf = map_cluster(smem_u32(sm + V_PBUF), peer);
+    const uint32_t peer_pfull = map_cluster(smem_u32(&c->pfull[0]), peer);
+    for (int t = 0; t < it.ntiles; ++t) {
+      const int s = t & 1;
+      const int k0 = it.k_begin + t * TK;
+      // Valid-key bits of this tile: warp w covers keys 32w .. 32w+31.
+      {
+        const int kp = k0 + 32 * w + lane;
+        bool v = false;
+        if (kp < it.k_end) {
+          const int id = __ldg(a.kv_indices + it.loc.idx_base + kp);
+          v = id >= 0 && (a.pool_rows <= 0 || id < a.pool_rows);
+          if (!v) atomicOr(a.status, DDTREE_ST_BAD_INDEX);
+        }
+        const uint32_t bits = __ballot_sync(0xffffffffu, v);
+        if (lane == 0) c->key_mask[s][w] = bits;
+      }
+      wait_or_abort(&c->sfull[s], (t >> 1) & 1, c, a.status);  // on expiry: continue, stop below
+      tc_fence_after();
+      float x[TK];
+      {
+        uint32_t v[16];
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+          tmem_ld16(tmem + my_lane_addr + 256 + 128 * s + 16 * q, v);
+          tmem_ld_wait();
+#pragma unroll
+          for (int e = 0; e < 16; ++e) x[16 * q + e] = __uint_as_float(v[e]);
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&c->sempty[s]);
+      named_bar(1, 128);  // key_mask of this tile visible; previous tile's staging reads done
+      uint32_t km[4];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) km[q] = c->key_mask[s][q];
+      float mt = -INFINITY;
+#pragma unroll
+      for (int k = 0; k < TK; ++k) {
+        const int kp = k0 + k;
+        bool ok = row_ok && ((km[k >> 5] >> (k & 31)) & 1u);
+        if (ok && kp >= it.loc.P) ok = (anc >> (kp - it.loc.P)) & 1ull;
+        x[k] = ok ? x[k] * scale2 : -INFINITY;
+        mt = fmaxf(mt, x[k]);
+      }
+      float alpha = 1.f;
+      if (mt > m_ref + kLazyRescale) {  // also true on the first finite max
+        alpha = (m_ref == -INFINITY) ? 0.f : exp2f(m_ref - mt);
+        m_ref = mt;
+      }
+      // Staging buffer s is free once the copy of tile t-2 has read it.
+      if (r == 0) asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
+      named_bar(1, 128);
+      uint8_t* stg = sm + Q_STAGE + s * PBUF;
+      float sum = 0.f;
+#pragma unroll
+      for (int cc = 0; cc < 16; ++cc) {  // 16-byte chunk cc = keys 8cc .. 8cc+7
+        uint32_t pk[4];
+#pragma unroll
+        for (int h = 0; h < 4; ++h) {
+          const float p0 = (m_ref == -INFINITY) ? 0.f : exp2f(x[8 * cc + 2 * h] - m_ref);
+          const float p1 = (m_ref == -INFINITY) ? 0.f : exp2f(x[8 * cc + 2 * h + 1] - m_ref);
+          __nv_bfloat162 b = __floats2bfloat162_rn(p0, p1);
+          sum += __low2float(b) + __high2float(b);
+          pk[h] = *reinterpret_cast<uint32_t*>(&b);
+        }
+        const int atom = cc >> 3, c16 = cc & 7;
+        *reinterpret_cast<uint4*>(stg + atom * CHUNK + r * 128 + ((c16 ^ (r & 7)) << 4)) =
+            make_uint4(pk[0], pk[1], pk[2], pk[3]);
+      }
+      l = l * alpha + sum;
+      float* meta = reinterpret_cast<float*>(stg + PTILE);
+      meta[r] = alpha;
+      meta[128 + r] = l;
+      const uint32_t flag = __ballot_sync(0xffffffffu, t > 0 && alpha != 1.f);
+      if (lane == 0) reinterpret_cast<uint32_t*>(meta + 256)[w] = flag;
+      fence_async_smem();
+      named_bar(1, 128);
+      if (r == 0 && !aborted(c)) {
+        // The peer's P buffer s is free once it finished tile t-2.
+        if (wait_cluster_or_abort(&c->pfree[s], ((t >> 1) & 1) ^ 1, c, a.status)) {
+          asm volatile(
+              "cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];\n"
+              "cp.async.bulk.commit_group;" ::"r"(peer_pbuf + s * PBUF),
+              "r"(smem_u32(stg)), "r"(PCOPY), "r"(peer_pfull + s * 8)
+              : "memory");
+        }
+      }
+      if (named_bar_or(1, 128, aborted(c))) break;
+    }
+    if (row_ok) {
+      a.partial_lse[(size_t)it.slot * a.rows_per_req + req_row] =
+          (l > 0.f) ? (m_ref + log2f(l)) * 0.6931471805599453f : -INFINITY;
+    }
+    if (r == 0) asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+  }
+}
+
+// ------------------------------------------------------------ accumulator
+__device__ void accumulator(const VerifyArgs& a, const Item& it, uint8_t* sm, Ctrl* c) {
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const uint32_t tmem = c->tmem_base;  // O: cols [0,512)
+  const uint32_t peer = 0;
+
+  if (warp == 0) {
+    // ---- producer: value chunks (0,1), (2,3), (4,5), (6,7) of every tile
+    int32_t idx[32];
+    int n = 0;
+    for (int t = 0; t < it.ntiles; ++t) {
+      load_tile_indices(a, it, t, lane, idx);
+      for (int q = 0; q < 4; ++q, ++n) {
+        const int slot = n % VRING;
+        if (!wait_or_abort(&c->vempty[slot], ((n / VRING) & 1) ^ 1, c, a.status)) {
+          asm volatile("cp.async.wait_all;" ::: "memory");
+          return;
+        }
+        gather_chunks(sm + V_RING + slot * 2 * CHUNK, a.kv_pool, idx, 2 * q, 2, lane, &c->vfull[slot]);
+      }
+    }
+  } else if (warp == 1) {
+    // ---- MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t idesc = idesc_bf16_f32(128, 128, false, true);  // A = P K-major, B = V MN-major
+      for (int s = 0; s < 2; ++s) mbar_arrive_expect_tx(&c->pfull[s], PCOPY);
+      int n = 0;
+      uint32_t corr_ph = 0;
+      bool ok = true;
+      for (int t = 0; t < it.ntiles && ok; ++t) {
+        const int s = t & 1;
+        if (!wait_or_abort(&c->pfull[s], (t >> 1) & 1, c, a.status)) { ok = false; break; }
+        const uint32_t* flags = reinterpret_cast<const uint32_t*>(sm + V_PBUF + s * PBUF + PTILE + 1024);
+        if (flags[0] | flags[1] | flags[2] | flags[3]) {
+          if (!wait_or_abort(&c->corr_done, corr_ph, c, a.status)) { ok = false; break; }
+          corr_ph ^= 1;
+        }
+        tc_fence_after();
+        const uint64_t pdesc = desc_sw128(smem_u32(sm + V_PBUF + s * PBUF), 16, 1024);
+        for (int q = 0; q < 4; ++q, ++n) {
+          const int slot = n % VRING;
+          if (!wait_or_abort(&c->vfull[slot], (n / VRING) & 1, c, a.status)) { ok = false; break; }
+          fence_async_smem();  // cp.async (generic proxy) data -> tensor-core reads
+          tc_fence_after();
+          const uint64_t vdesc = desc_sw128(smem_u32(sm + V_RING + slot * 2 * CHUNK), CHUNK, 1024);
+#pragma unroll
+          for (int ks = 0; ks < 8; ++ks) {
+            const uint64_t ad = pdesc + (uint64_t)(((ks >> 2) * CHUNK + (ks & 3) * 32) >> 4);
+            const uint64_t bd = vdesc + (uint64_t)((ks * 2048) >> 4);
+            mma_ss(tmem + 128 * q, ad, bd, idesc, (t > 0 || ks > 0) ? 1u : 0u);
+          }
+          mma_commit(&c->vempty[slot]);
+        }
+        if (ok) mma_commit(&c->pvdone[s]);
+      }
+      mma_commit(&c->mma_done);
+    }
+  } else if (warp == 2) {
+    // ---- relay: when PV of tile t finished, re-arm the P buffer and tell
+    // the scorer (first of its two releases of that buffer).
+    if (lane == 0) {
+      const uint32_t peer_pfree = map_cluster(smem_u32(&c->pfree[0]), peer);
+      for (int t = 0; t < it.ntiles; ++t) {
+        const int s = t & 1;
+        if (!wait_or_abort(&c->pvdone[s], (t >> 1) & 1, c, a.status)) break;
+        if (t + 2 < it.ntiles) mbar_arrive_expect_tx(&c->pfull[s], PCOPY);
+        asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(peer_pfree + s * 8)
+                     : "memory");
+      }
+    }
+  } else if (warp >= 4) {
+    // ---- correction + epilogue: thread = row r (TMEM lane r)
+    const int r = tid - 128;
+    const int w = warp - 4;
+    const uint32_t lane_addr = tmem + ((uint32_t)(w * 32) << 16);
+    const uint32_t peer_pfree = map_cluster(smem_u32(&c->pfree[0]), peer);
+    float lfin = 0.f;
+    for (int t = 0; t < it.ntiles; ++t) {
+      const int s = t & 1;
+      wait_or_abort(&c->pfull[s], (t >> 1) & 1, c, a.status);  // on expiry: continue, stop below
+      const uint8_t* pb = sm + V_PBUF + s * PBUF;
+      const float* meta = reinterpret_cast<const float*>(pb + PTILE);
+      const uint32_t* flags = reinterpret_cast<const uint32_t*>(meta + 256);
+      lfin = meta[128 + r];
+      if (flags[0] | flags[1] | flags[2] | flags[3]) {
+        const float alpha = meta[r];
+        // O must hold PV of tiles < t before it is rescaled.
+        wait_or_abort(&c->pvdone[(t - 1) & 1], ((t - 1) >> 1) & 1, c, a.status);
+        tc_fence_after();
+        // tcgen05.ld/st are warp-collective: the whole warp takes part when
+        // any of its rows needs rescaling (alpha == 1 leaves a row unchanged).
+        if (__any_sync(0xffffffffu, alpha != 1.f)) {
+          uint32_t v[16];
+          for (int q = 0; q < 32; ++q) {
+            tmem_ld16(lane_addr + 16 * q, v);
+            tmem_ld_wait();
+#pragma unroll
+            for (int e = 0; e < 16; ++e) v[e] = __float_as_uint(__uint_as_float(v[e]) * alpha);
+            tmem_st16(lane_addr + 16 * q, v);
+          }
+          tmem_st_wait();
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&c->corr_done);
+      }
+      // Second release of P buffer s: its metadata has been read.
+      const bool stop = named_bar_or(2, 128, aborted(c));
+      if (r == 0 && !stop)
+        asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(peer_pfree + s * 8)
+                     : "memory");
+      if (stop) break;
+    }
+    // Epilogue: O_s = O / l, written as fp32 rows of the workspace.
+    const bool done = wait_or_abort(&c->mma_done, 0, c, a.status);
+    tc_fence_after();
+    const int req_row = it.row0 + r;
+    const bool row_ok = req_row < a.rows_per_req;
+    // `done` is the same for every thread (all wait on one phase, or all see
+    // the abort flag); the TMEM loads are warp-collective, the stores per row.
+    if (__all_sync(0xffffffffu, done)) {
+      const float inv = lfin > 0.f ? 1.f / lfin : 0.f;
+      float* po = a.partial_o + ((size_t)it.slot * a.rows_per_req + (row_ok ? req_row : 0)) * kLatent;
+      uint32_t v[16];
+      for (int q = 0; q < 32; ++q) {
+        tmem_ld16(lane_addr + 16 * q, v);
+        tmem_ld_wait();
+        if (row_ok) {
+#pragma unroll
+          for (int e = 0; e < 16; e += 4)
+            *reinterpret_cast<float4*>(po + 16 * q + e) =
+                make_float4(__uint_as_float(v[e]) * inv, __uint_as_float(v[e + 1]) * inv,
+                            __uint_as_float(v[e + 2]) * inv, __uint_as_float(v[e + 3]) * inv);
+        }
+      }
+    } else if (row_ok) {
+      for (int d = 0; d < kLatent; ++d)
+        a.partial_o[((size_t)it.slot * a.rows_per_req + req_row) * kLatent + d] = 0.f;
+    }
+  }
+}
+
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
+    partial_tc_kernel(const VerifyArgs a) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* sm = reinterpret_cast<uint8_t*>(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+  Ctrl* c = reinterpret_cast<Ctrl*>(sm + BIG_END);
+  const int tid = threadIdx.x, warp = tid >> 5;
+  const uint32_t role = cluster_ctarank();
+  const int pair = blockIdx.x >> 1;
+
+  Item it;
+  const int row_tile = pair % a.row_tiles;
+  it.slot = pair / a.row_tiles;
+  const bool have = locate_split(a, it.slot, it.loc);
+  it.row0 = row_tile * ROWS;
+  it.k_begin = have ? it.loc.s * a.chunk_keys : 0;
+  it.k_end = have ? min(it.k_begin + a.chunk_keys, it.loc.nkeys) : 0;
+  it.ntiles = have ? (it.k_end - it.k_begin + TK - 1) / TK : 0;
+  // Both CTAs of a cluster see the same item; an empty item skips all work
+  // but still takes part in the cluster barriers.
+
+  if (tid == 0) {
+    for (int i = 0; i < QRING; ++i) { mbar_init(&c->kfull[i], 32); mbar_init(&c->kempty[i], 1); }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&c->sfull[i], 1);
+      mbar_init(&c->sempty[i], 4);
+      mbar_init(&c->pfree[i], 2);
+      mbar_init(&c->pfull[i], 1);
+      mbar_init(&c->pvdone[i], 1);
+    }
+    for (int i = 0; i < VRING; ++i) { mbar_init(&c->vfull[i], 32); mbar_init(&c->vempty[i], 1); }
+    mbar_init(&c->corr_done, 4);
+    mbar_init(&c->mma_done, 1);
+    c->abort = 0;
+    fence_mbar_init();
+  }
+  if (warp == 3) {
+    tmem_alloc(&c->tmem_base, 512);
+    tmem_relinquish();
+  }
+  if (role == 0 && have) {
+    const int T = a.n_nodes;
+    if (tid < T) c->anc[tid] = ancestor_bits(a.tree_parent + (size_t)it.loc.b * T, tid, T, a.status);
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+
+  if (role == 0 && have && warp >= 4) {
+    // Q rows -> TMEM (latent, packed bf16 pairs) and shared memory (rope).
+    const int r = tid - 128;
+    const int req_row = it.row0 + r;
+    const bool ok = req_row < a.rows_per_req;
+    const size_t g = (size_t)it.loc.b * a.rows_per_req + req_row;
+    const uint4* ql = reinterpret_cast<const uint4*>(a.q_latent + g * a.q_lat_stride);
+    const uint32_t lane_addr = c->tmem_base + ((uint32_t)((warp - 4) * 32) << 16);
+    for (int q = 0; q < 16; ++q) {  // 16 x 16 columns = 512 bf16
+      uint32_t v[16];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        uint4 x = ok ? __ldg(ql + 4 * q + e) : make_uint4(0, 0, 0, 0);
+        v[4 * e] = x.x; v[4 * e + 1] = x.y; v[4 * e + 2] = x.z; v[4 * e + 3] = x.w;
+      }
+      tmem_st16(lane_addr + 16 * q, v);
+    }
+    tmem_st_wait();
+    const uint4* qr = reinterpret_cast<const uint4*>(a.q_rope + g * a.q_rope_stride);
+#pragma unroll
+    for (int c16 = 0; c16 < 8; ++c16) {
+      uint4 x = ok ? __ldg(qr + c16) : make_uint4(0, 0, 0, 0);
+      *reinterpret_cast<uint4*>(sm + Q_ROPE + r * 128 + ((c16 ^ (r & 7)) << 4)) = x;
+    }
+    fence_async_smem();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  cluster_sync();  // both CTAs' barriers initialised before any remote traffic
+
+  if (have && it.ntiles > 0) {
+    if (role == 0) scorer(a, it, sm, c);
+    else accumulator(a, it, sm, c);
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  // Tensor-core work of this CTA must be finished before TMEM is freed.
+  if (warp == 3 && have && it.ntiles > 0) {
+    mbar_wait(&c->mma_done, 0, global_timer_ns() + kWaitNs);
+  }
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync();  // no remote copy or arrival may target a CTA that has exited
+  tc_fence_after();
+  if (warp == 3) tmem_dealloc(c->tmem_base, 512);
+}
+
+}  // namespace
+
+cudaError_t launch_partial_tc(const VerifyArgs& a, cudaStream_t stream) {
+  static bool attr_set[64] = {};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64 || !attr_set[dev]) {
+    e = cudaFuncSetAttribute(partial_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
+    if (e != cudaSuccess) return e;
+    if (dev >= 0 && dev < 64) attr_set[dev] = true;
+  }
+  dim3 grid(2 * a.row_tiles * a.total_splits);
+  partial_tc_kernel<<<grid, kThreads, kSmemBytes, stream>>>(a);
+  return cudaGetLastError();
+}
+
 }  // namespace ddtree
