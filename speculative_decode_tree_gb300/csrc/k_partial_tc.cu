@@ -8,8 +8,10 @@
 //  scorer (cluster rank 0)
 //    Q latent (128 x 512 bf16) lives in TMEM as the A operand, Q rope in
 //    shared memory; per tile of 128 keys it gathers the 576-wide key rows
-//    through the page_size=1 index table with 16-byte cp.async into
-//    128-byte-swizzled chunks of 64 columns ("Chunk 66.1": 128-bit loads),
+//    through the page_size=1 index table with TMA row gathers (4 rows per
+//    instruction, "Chunk 66.1": wide KV loads) into 128-byte-swizzled chunks
+//    of 64 columns, or with one 2-D TMA tile load per chunk when the tile's
+//    128 indices are one contiguous run (defragmented KV),
 //    issues S = Q K^T (M=128, N=128, K=576) into one of two TMEM S buffers,
 //    and four softmax warps (one query row per thread) apply the ancestor
 //    mask on tree keys only, keep a running max with lazy rescaling, and
@@ -27,6 +29,8 @@
 // Every mbarrier wait is bounded; on expiry the kernel sets
 // DDTREE_ST_TIMEOUT, stops issuing work, waits (bounded) for its own
 // tensor-core work and frees its TMEM.
+#include <cuda.h>
+
 #include "common.cuh"
 #include "tc_ptx.cuh"
 
@@ -44,7 +48,7 @@ constexpr int PTILE = 32768;            // bf16 P tile: 2 swizzle atoms of 128 r
 constexpr int META = 1040;              // alpha[128], lfin[128], flag words[4]
 constexpr int PCOPY = PTILE + META;     // bytes shipped per tile (multiple of 16)
 constexpr int PBUF = 34816;             // P buffer stride (1024-aligned)
-constexpr int kThreads = 256;
+constexpr int kThreads = 384;                  // 12 warps
 constexpr float kLazyRescale = 8.0f;    // rescale only when the max grows by > 2^8 (log2 units)
 constexpr uint64_t kWaitNs = 2000000000ull;
 
@@ -70,6 +74,7 @@ struct __align__(8) Ctrl {
   uint32_t tmem_base;
   uint32_t abort;
   uint32_t key_mask[2][4];               // scorer: valid-key bits per tile parity
+  uint32_t pad_;
   uint64_t anc[64];                      // scorer: ancestor bits per node
 };
 
@@ -113,27 +118,6 @@ __device__ __forceinline__ bool named_bar_or(int id, int nthreads, bool pred) {
 }
 __device__ __forceinline__ bool aborted(Ctrl* c) { return *(volatile uint32_t*)&c->abort != 0; }
 
-// Gathers `nchunks` consecutive 64-column chunks (starting at column chunk
-// c0) of the tile's 128 key rows into `dst` (chunk stride CHUNK), 128-byte
-// swizzled, then arrives on `bar` when the copies land.  Lane l handles key
-// rows (l >> 3) + 4 i and 16-byte piece (l & 7) of each 128-byte chunk row.
-__device__ __forceinline__ void gather_chunks(uint8_t* dst, const uint16_t* pool, const int32_t (&idx)[32],
-                                              int c0, int nchunks, int lane, uint64_t* bar) {
-  const int piece = lane & 7;
-  for (int c = 0; c < nchunks; ++c) {
-    const uint32_t base = smem_u32(dst + c * CHUNK);
-#pragma unroll 8
-    for (int i = 0; i < 32; ++i) {
-      const int key = (lane >> 3) + 4 * i;
-      const int id = idx[i];
-      const uint32_t d = base + key * 128 + ((piece ^ (key & 7)) << 4);
-      const uint16_t* src = pool + (size_t)(id < 0 ? 0 : id) * kRow + (c0 + c) * 64 + piece * 8;
-      cp_async16_zfill(d, src, id < 0 ? 0u : 16u);
-    }
-  }
-  cp_async_mbar_arrive(bar);
-}
-
 struct Item {
   SplitLoc loc;
   int row0;      // first query row of the tile within the request
@@ -143,44 +127,157 @@ struct Item {
   int slot;      // split slot in the workspace
 };
 
-// Loads the tile's 128 indices for this lane (keys (lane>>3) + 4i); -1 for
-// keys past the chunk end or outside the pool (the latter flagged).
-__device__ __forceinline__ void load_tile_indices(const VerifyArgs& a, const Item& it, int tile, int lane,
-                                                  int32_t (&idx)[32]) {
-  const int k0 = it.k_begin + tile * TK;
+// TMA maps of the KV pool: rows of 576 bf16, 128-byte swizzle; `row4` has a
+// one-row box for tile::gather4, `tile` a 128-row box for contiguous runs.
+struct PoolMaps {
+  CUtensorMap row4;
+  CUtensorMap tile;
+};
+
+// One tile's 128 key indices as this lane sees them: keys 4*lane .. 4*lane+3
+// (out-of-range and past-the-chunk keys become -1, which TMA fills with
+// zeros), plus whether the whole tile is one contiguous, fully valid run.
+struct TileIdx {
+  int4 k4;
+  int first;
+  bool contiguous;
+};
+
+__device__ __forceinline__ TileIdx load_tile_indices(const VerifyArgs& a, const Item& it, int tile, int lane) {
+  const int k0 = it.k_begin + tile * TK + 4 * lane;
+  int v[4];
 #pragma unroll
-  for (int i = 0; i < 32; ++i) {
-    const int kp = k0 + (lane >> 3) + 4 * i;
+  for (int j = 0; j < 4; ++j) {
     int id = -1;
-    if (kp < it.k_end) {
-      id = __ldg(a.kv_indices + it.loc.idx_base + kp);
+    if (k0 + j < it.k_end) {
+      id = __ldg(a.kv_indices + it.loc.idx_base + k0 + j);
       if (id < 0 || (a.pool_rows > 0 && id >= a.pool_rows)) id = -1;
     }
-    idx[i] = id;
+    v[j] = id;
   }
+  TileIdx t;
+  t.k4 = make_int4(v[0], v[1], v[2], v[3]);
+  t.first = __shfl_sync(0xffffffffu, v[0], 0);
+  const bool run = v[0] >= 0 && v[0] == t.first + 4 * lane && v[1] == v[0] + 1 && v[2] == v[0] + 2 &&
+                   v[3] == v[0] + 3;
+  t.contiguous = __all_sync(0xffffffffu, run);
+  return t;
+}
+
+// Producer warps.  Scorer: warps 0, 2, 3, 8..11 (7); accumulator: warps 0, 3,
+// 8..11 (6).  Returns the producer rank of `warp`, or -1.
+constexpr int kScorerProducers = 7;
+constexpr int kAccProducers = 6;
+__device__ __forceinline__ int producer_rank(int warp, bool scorer) {
+  if (warp == 0) return 0;
+  if (scorer && warp == 2) return 1;
+  if (warp == 3) return scorer ? 2 : 1;
+  if (warp >= 8) return warp - (scorer ? 5 : 6);
+  return -1;
+}
+
+// The key indices this producer lane copies for its four-key groups
+// g = rank, rank + np, ... (lane covers key 4g + lane/8, 16-byte piece lane%8).
+struct MyKeys {
+  int id[6];  // ceil(32 / producers) groups at most
+  int n;
+};
+__device__ __forceinline__ MyKeys my_keys(const TileIdx& ti, int lane, int rank, int np) {
+  MyKeys mk;
+  mk.n = 0;
+  const int sel = lane >> 3;
+#pragma unroll
+  for (int j = 0; j < 6; ++j) {
+    const int g = rank + j * np;
+    const int x = __shfl_sync(0xffffffffu, ti.k4.x, g & 31);
+    const int y = __shfl_sync(0xffffffffu, ti.k4.y, g & 31);
+    const int z = __shfl_sync(0xffffffffu, ti.k4.z, g & 31);
+    const int w = __shfl_sync(0xffffffffu, ti.k4.w, g & 31);
+    mk.id[j] = sel == 0 ? x : sel == 1 ? y : sel == 2 ? z : w;
+    if (g < 32) mk.n = j + 1;
+  }
+  return mk;
+}
+
+// Fills `nchunks` 64-column chunks (columns 64*c0 ...) of the tile into
+// `dst` (chunk stride CHUNK; row k at +128 k, 128-byte swizzled) and arrives
+// on `bar` once per lane.  Scattered tiles: 16-byte cp.async of this warp's
+// key groups (zero-filled for invalid keys).  Contiguous tiles: rank 0 adds
+// the bytes to `bar` and loads each chunk with one 2-D TMA tile; the others
+// only arrive.  `bar` expects 32 arrivals per producer warp.
+__device__ __forceinline__ void fill_chunks(const PoolMaps& maps, const uint16_t* pool, uint8_t* dst, int c0,
+                                            int nchunks, const TileIdx& ti, const MyKeys& mk, int rank, int np,
+                                            int lane, uint64_t* bar) {
+  if (ti.contiguous) {
+    if (rank == 0 && lane == 0) {
+      mbar_expect_tx(bar, nchunks * CHUNK);
+      for (int c = 0; c < nchunks; ++c)
+        asm volatile(
+            "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];"
+            ::"r"(smem_u32(dst + c * CHUNK)), "l"(&maps.tile), "r"((c0 + c) * 64), "r"(ti.first),
+              "r"(smem_u32(bar))
+            : "memory");
+    }
+    __syncwarp();
+  } else {
+    const int piece = lane & 7;
+    for (int c = 0; c < nchunks; ++c) {
+      const uint32_t base = smem_u32(dst + c * CHUNK);
+#pragma unroll
+      for (int j = 0; j < 6; ++j) {
+        if (j < mk.n) {
+          const int key = 4 * (rank + j * np) + (lane >> 3);
+          const int id = mk.id[j];
+          const uint16_t* src = pool + (size_t)(id < 0 ? 0 : id) * kRow + (c0 + c) * 64 + piece * 8;
+          cp_async16_zfill(base + key * 128 + ((piece ^ (key & 7)) << 4), src, id < 0 ? 0u : 16u);
+        }
+      }
+    }
+  }
+  cp_async_mbar_arrive(bar);
+}
+
+// Pulls the whole 1152-byte rows of one tile's keys into L2 with one bulk
+// prefetch per row (through this SM's otherwise idle TMA unit); thread r of
+// 128 handles key r.  Issued by the accumulator a few tiles ahead
+// of the scorer, so the scorer's gathers hit L2 instead of waiting on DRAM.
+constexpr int kL2Ahead = 3;
+__device__ __forceinline__ void prefetch_tile_l2(const VerifyArgs& a, const Item& it, int tile, int r) {
+  if (tile >= it.ntiles) return;
+  const int kp = it.k_begin + tile * TK + r;
+  if (kp >= it.k_end) return;
+  const int id = __ldg(a.kv_indices + it.loc.idx_base + kp);
+  if (id < 0 || (a.pool_rows > 0 && id >= a.pool_rows)) return;
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(a.kv_pool + (size_t)id * kRow), "r"(kRow * 2)
+               : "memory");
 }
 
 // ------------------------------------------------------------------ scorer
-__device__ void scorer(const VerifyArgs& a, const Item& it, uint8_t* sm, Ctrl* c) {
+__device__ void scorer(const VerifyArgs& a, const PoolMaps& maps, const Item& it, uint8_t* sm, Ctrl* c) {
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const uint32_t tmem = c->tmem_base;        // cols [0,256): Q latent; [256,384), [384,512): S
   const uint32_t peer = 1;
 
-  if (warp == 0) {
-    // ---- producer: key chunks 0..8 of every tile
-    int32_t idx[32];
+  const int prank = producer_rank(warp, true);
+  if (prank >= 0) {
+    // ---- producers: key chunks 0..8 of every tile
     int n = 0;
     for (int t = 0; t < it.ntiles; ++t) {
-      load_tile_indices(a, it, t, lane, idx);
+      const TileIdx ti = load_tile_indices(a, it, t, lane);
+      const MyKeys mk = my_keys(ti, lane, prank, kScorerProducers);
       for (int ch = 0; ch < 9; ++ch, ++n) {
         const int slot = n % QRING;
-        if (!wait_or_abort(&c->kempty[slot], ((n / QRING) & 1) ^ 1, c, a.status)) {
+        bool ok = true;
+        if (lane == 0) ok = wait_or_abort(&c->kempty[slot], ((n / QRING) & 1) ^ 1, c, a.status);
+        if (!__shfl_sync(0xffffffffu, ok, 0)) {
           asm volatile("cp.async.wait_all;" ::: "memory");
           return;
         }
-        gather_chunks(sm + Q_RING + slot * CHUNK, a.kv_pool, idx, ch, 1, lane, &c->kfull[slot]);
+        fill_chunks(maps, a.kv_pool, sm + Q_RING + slot * CHUNK, ch, 1, ti, mk, prank, kScorerProducers, lane,
+                    &c->kfull[slot]);
       }
     }
+    asm volatile("cp.async.wait_all;" ::: "memory");
   } else if (warp == 1) {
     // ---- MMA issuer (one thread)
     if (lane == 0) {
@@ -241,17 +338,9 @@ __device__ void scorer(const VerifyArgs& a, const Item& it, uint8_t* sm, Ctrl* c
       }
       wait_or_abort(&c->sfull[s], (t >> 1) & 1, c, a.status);  // on expiry: continue, stop below
       tc_fence_after();
-      float x[TK];
-      {
-        uint32_t v[16];
+      uint32_t xr[4][32];  // raw fp32 scores of this row, 128 keys
 #pragma unroll
-        for (int q = 0; q < 8; ++q) {
-          tmem_ld16(tmem + my_lane_addr + 256 + 128 * s + 16 * q, v);
-          tmem_ld_wait();
-#pragma unroll
-          for (int e = 0; e < 16; ++e) x[16 * q + e] = __uint_as_float(v[e]);
-        }
-      }
+      for (int q = 0; q < 4; ++q) tmem_ld32(tmem + my_lane_addr + 256 + 128 * s + 32 * q, xr[q]);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&c->sempty[s]);
@@ -259,40 +348,53 @@ __device__ void scorer(const VerifyArgs& a, const Item& it, uint8_t* sm, Ctrl* c
       uint32_t km[4];
 #pragma unroll
       for (int q = 0; q < 4; ++q) km[q] = c->key_mask[s][q];
-      float mt = -INFINITY;
+      // Tiles of valid prefix keys only (the common case) need no mask.
+      const bool plain = (k0 + TK <= it.loc.P) && (k0 + TK <= it.k_end) &&
+                         ((km[0] & km[1] & km[2] & km[3]) == 0xffffffffu);
+      float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+      if (plain && row_ok) {
 #pragma unroll
-      for (int k = 0; k < TK; ++k) {
-        const int kp = k0 + k;
-        bool ok = row_ok && ((km[k >> 5] >> (k & 31)) & 1u);
-        if (ok && kp >= it.loc.P) ok = (anc >> (kp - it.loc.P)) & 1ull;
-        x[k] = ok ? x[k] * scale2 : -INFINITY;
-        mt = fmaxf(mt, x[k]);
+        for (int k = 0; k < TK; ++k) mx[k & 3] = fmaxf(mx[k & 3], __uint_as_float(xr[k >> 5][k & 31]));
+      } else {
+#pragma unroll
+        for (int k = 0; k < TK; ++k) {
+          const int kp = k0 + k;
+          bool ok = row_ok && ((km[k >> 5] >> (k & 31)) & 1u);
+          if (ok && kp >= it.loc.P) ok = (anc >> (kp - it.loc.P)) & 1ull;
+          const float v = ok ? __uint_as_float(xr[k >> 5][k & 31]) : -INFINITY;
+          xr[k >> 5][k & 31] = __float_as_uint(v);
+          mx[k & 3] = fmaxf(mx[k & 3], v);
+        }
       }
+      const float mt = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])) * scale2;
       float alpha = 1.f;
       if (mt > m_ref + kLazyRescale) {  // also true on the first finite max
-        alpha = (m_ref == -INFINITY) ? 0.f : exp2f(m_ref - mt);
+        alpha = (m_ref == -INFINITY) ? 0.f : ex2_approx(m_ref - mt);
         m_ref = mt;
       }
+      const float nm = (m_ref == -INFINITY) ? 0.f : -m_ref;
       // Staging buffer s is free once the copy of tile t-2 has read it.
       if (r == 0) asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
       named_bar(1, 128);
       uint8_t* stg = sm + Q_STAGE + s * PBUF;
-      float sum = 0.f;
+      float ps[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
       for (int cc = 0; cc < 16; ++cc) {  // 16-byte chunk cc = keys 8cc .. 8cc+7
         uint32_t pk[4];
 #pragma unroll
         for (int h = 0; h < 4; ++h) {
-          const float p0 = (m_ref == -INFINITY) ? 0.f : exp2f(x[8 * cc + 2 * h] - m_ref);
-          const float p1 = (m_ref == -INFINITY) ? 0.f : exp2f(x[8 * cc + 2 * h + 1] - m_ref);
+          const int k = 8 * cc + 2 * h;
+          const float p0 = ex2_approx(fmaf(__uint_as_float(xr[k >> 5][k & 31]), scale2, nm));
+          const float p1 = ex2_approx(fmaf(__uint_as_float(xr[(k + 1) >> 5][(k + 1) & 31]), scale2, nm));
+          ps[h] += p0 + p1;
           __nv_bfloat162 b = __floats2bfloat162_rn(p0, p1);
-          sum += __low2float(b) + __high2float(b);
           pk[h] = *reinterpret_cast<uint32_t*>(&b);
         }
         const int atom = cc >> 3, c16 = cc & 7;
         *reinterpret_cast<uint4*>(stg + atom * CHUNK + r * 128 + ((c16 ^ (r & 7)) << 4)) =
             make_uint4(pk[0], pk[1], pk[2], pk[3]);
       }
+      const float sum = (row_ok ? 1.f : 0.f) * ((ps[0] + ps[1]) + (ps[2] + ps[3]));
       l = l * alpha + sum;
       float* meta = reinterpret_cast<float*>(stg + PTILE);
       meta[r] = alpha;
@@ -322,26 +424,31 @@ __device__ void scorer(const VerifyArgs& a, const Item& it, uint8_t* sm, Ctrl* c
 }
 
 // ------------------------------------------------------------ accumulator
-__device__ void accumulator(const VerifyArgs& a, const Item& it, uint8_t* sm, Ctrl* c) {
+__device__ void accumulator(const VerifyArgs& a, const PoolMaps& maps, const Item& it, uint8_t* sm, Ctrl* c) {
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const uint32_t tmem = c->tmem_base;  // O: cols [0,512)
   const uint32_t peer = 0;
 
-  if (warp == 0) {
-    // ---- producer: value chunks (0,1), (2,3), (4,5), (6,7) of every tile
-    int32_t idx[32];
+  const int prank = producer_rank(warp, false);
+  if (prank >= 0) {
+    // ---- producers: value chunk pairs (0,1) .. (6,7) of every tile
     int n = 0;
     for (int t = 0; t < it.ntiles; ++t) {
-      load_tile_indices(a, it, t, lane, idx);
+      const TileIdx ti = load_tile_indices(a, it, t, lane);
+      const MyKeys mk = my_keys(ti, lane, prank, kAccProducers);
       for (int q = 0; q < 4; ++q, ++n) {
         const int slot = n % VRING;
-        if (!wait_or_abort(&c->vempty[slot], ((n / VRING) & 1) ^ 1, c, a.status)) {
+        bool ok = true;
+        if (lane == 0) ok = wait_or_abort(&c->vempty[slot], ((n / VRING) & 1) ^ 1, c, a.status);
+        if (!__shfl_sync(0xffffffffu, ok, 0)) {
           asm volatile("cp.async.wait_all;" ::: "memory");
           return;
         }
-        gather_chunks(sm + V_RING + slot * 2 * CHUNK, a.kv_pool, idx, 2 * q, 2, lane, &c->vfull[slot]);
+        fill_chunks(maps, a.kv_pool, sm + V_RING + slot * 2 * CHUNK, 2 * q, 2, ti, mk, prank, kAccProducers, lane,
+                    &c->vfull[slot]);
       }
     }
+    asm volatile("cp.async.wait_all;" ::: "memory");
   } else if (warp == 1) {
     // ---- MMA issuer
     if (lane == 0) {
@@ -398,8 +505,10 @@ __device__ void accumulator(const VerifyArgs& a, const Item& it, uint8_t* sm, Ct
     const uint32_t lane_addr = tmem + ((uint32_t)(w * 32) << 16);
     const uint32_t peer_pfree = map_cluster(smem_u32(&c->pfree[0]), peer);
     float lfin = 0.f;
+    for (int t = 0; t < kL2Ahead; ++t) prefetch_tile_l2(a, it, t, r);
     for (int t = 0; t < it.ntiles; ++t) {
       const int s = t & 1;
+      prefetch_tile_l2(a, it, t + kL2Ahead, r);
       wait_or_abort(&c->pfull[s], (t >> 1) & 1, c, a.status);  // on expiry: continue, stop below
       const uint8_t* pb = sm + V_PBUF + s * PBUF;
       const float* meta = reinterpret_cast<const float*>(pb + PTILE);
@@ -416,7 +525,6 @@ __device__ void accumulator(const VerifyArgs& a, const Item& it, uint8_t* sm, Ct
           uint32_t v[16];
           for (int q = 0; q < 32; ++q) {
             tmem_ld16(lane_addr + 16 * q, v);
-            tmem_ld_wait();
 #pragma unroll
             for (int e = 0; e < 16; ++e) v[e] = __float_as_uint(__uint_as_float(v[e]) * alpha);
             tmem_st16(lane_addr + 16 * q, v);
@@ -447,7 +555,6 @@ __device__ void accumulator(const VerifyArgs& a, const Item& it, uint8_t* sm, Ct
       uint32_t v[16];
       for (int q = 0; q < 32; ++q) {
         tmem_ld16(lane_addr + 16 * q, v);
-        tmem_ld_wait();
         if (row_ok) {
 #pragma unroll
           for (int e = 0; e < 16; e += 4)
@@ -464,7 +571,7 @@ __device__ void accumulator(const VerifyArgs& a, const Item& it, uint8_t* sm, Ct
 }
 
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
-    partial_tc_kernel(const VerifyArgs a) {
+    partial_tc_kernel(const VerifyArgs a, const __grid_constant__ PoolMaps maps) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
   Ctrl* c = reinterpret_cast<Ctrl*>(sm + BIG_END);
@@ -484,7 +591,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   // but still takes part in the cluster barriers.
 
   if (tid == 0) {
-    for (int i = 0; i < QRING; ++i) { mbar_init(&c->kfull[i], 32); mbar_init(&c->kempty[i], 1); }
+    for (int i = 0; i < QRING; ++i) { mbar_init(&c->kfull[i], 32 * kScorerProducers); mbar_init(&c->kempty[i], 1); }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&c->sfull[i], 1);
       mbar_init(&c->sempty[i], 4);
@@ -492,7 +599,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       mbar_init(&c->pfull[i], 1);
       mbar_init(&c->pvdone[i], 1);
     }
-    for (int i = 0; i < VRING; ++i) { mbar_init(&c->vfull[i], 32); mbar_init(&c->vempty[i], 1); }
+    for (int i = 0; i < VRING; ++i) { mbar_init(&c->vfull[i], 32 * kAccProducers); mbar_init(&c->vempty[i], 1); }
     mbar_init(&c->corr_done, 4);
     mbar_init(&c->mma_done, 1);
     c->abort = 0;
@@ -510,8 +617,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
 
-  if (role == 0 && have && warp >= 4) {
-    // Q rows -> TMEM (latent, packed bf16 pairs) and shared memory (rope).
+  if (role == 0 && have && warp >= 4 && warp < 8) {
+    // Q rows -> TMEM (warps 4..7, thread = query row = TMEM lane): latent as
+    // packed bf16 pairs; rope -> shared memory.
     const int r = tid - 128;
     const int req_row = it.row0 + r;
     const bool ok = req_row < a.rows_per_req;
@@ -542,8 +650,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   cluster_sync();  // both CTAs' barriers initialised before any remote traffic
 
   if (have && it.ntiles > 0) {
-    if (role == 0) scorer(a, it, sm, c);
-    else accumulator(a, it, sm, c);
+    if (role == 0) scorer(a, maps, it, sm, c);
+    else accumulator(a, maps, it, sm, c);
   }
 
   tc_fence_before();
@@ -561,7 +669,57 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 
 }  // namespace
 
+namespace {
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+// cuTensorMapEncodeTiled from the driver, looked up once through the runtime
+// (the library does not link libcuda directly).
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  if (!fn) {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+    else
+      cudaGetLastError();
+  }
+  return fn;
+}
+
+// Pool maps over [rows, 576] bf16 with 1152-byte rows.  With an unknown pool
+// size the row extent is the int32 index range (the caller vouches for the
+// indices); otherwise rows past the pool read as zeros.
+cudaError_t make_pool_maps(const VerifyArgs& a, PoolMaps* m) {
+  EncodeTiledFn enc = encode_fn();
+  if (!enc) return cudaErrorNotSupported;
+  const cuuint64_t rows = a.pool_rows > 0 ? (cuuint64_t)a.pool_rows : (cuuint64_t)0x7fffffff;
+  const cuuint64_t dims[2] = {(cuuint64_t)kRow, rows};
+  const cuuint64_t strides[1] = {(cuuint64_t)kRow * 2};
+  const cuuint32_t box4[2] = {64, 1}, boxt[2] = {64, 128}, es[2] = {1, 1};
+  void* base = const_cast<uint16_t*>(a.kv_pool);
+  if (enc(&m->row4, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, base, dims, strides, box4, es,
+          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+    return cudaErrorInvalidValue;
+  if (enc(&m->tile, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, base, dims, strides, boxt, es,
+          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+    return cudaErrorInvalidValue;
+  return cudaSuccess;
+}
+
+}  // namespace
+
 cudaError_t launch_partial_tc(const VerifyArgs& a, cudaStream_t stream) {
+  PoolMaps maps;
+  cudaError_t me = make_pool_maps(a, &maps);
+  if (me != cudaSuccess) return me;
   static bool attr_set[64] = {};
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -572,7 +730,7 @@ cudaError_t launch_partial_tc(const VerifyArgs& a, cudaStream_t stream) {
     if (dev >= 0 && dev < 64) attr_set[dev] = true;
   }
   dim3 grid(2 * a.row_tiles * a.total_splits);
-  partial_tc_kernel<<<grid, kThreads, kSmemBytes, stream>>>(a);
+  partial_tc_kernel<<<grid, kThreads, kSmemBytes, stream>>>(a, maps);
   return cudaGetLastError();
 }
 
