@@ -43,7 +43,7 @@ def _args():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="long_scattered")
-    ap.add_argument("--kernel", choices=["auto", "simt", "tc"], default="auto")
+    ap.add_argument("--kernel", choices=["auto", "simt", "tc", "tc2"], default="auto")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-contiguous", action="store_true")
@@ -198,7 +198,7 @@ def run_ours(args, world, rank, local):
     peaks = _peaks()
     inp = workload(args.workload)
     cost = algorithmic_cost(inp)
-    kernel = {"auto": None, "simt": B.DDTREE_KERNEL_SIMT, "tc": B.DDTREE_KERNEL_TC}[args.kernel]
+    kernel = {"auto": None, "simt": B.DDTREE_KERNEL_SIMT, "tc": B.DDTREE_KERNEL_TC, "tc2": B.DDTREE_KERNEL_TC2}[args.kernel]
     dv = DeviceVerify(inp, device=str(dev), kernel=kernel)
     props = torch.cuda.get_device_properties(dev)
     l2 = getattr(props, "L2_cache_size", 128 << 20) or (128 << 20)
@@ -339,7 +339,7 @@ def run_ours(args, world, rank, local):
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": tc_peak, "unit": "TFLOP/s",
                      "frac": achieved / tc_peak, "traffic": None,
                      "peak_source": peaks["source"] + " bf16 burst (MEASURED_PEAKS.json)",
-                     "kernel": "split-KV partial (%s)" % ("tcgen05" if dv.plan.kernel == 2 else "simt")},
+                     "kernel": "split-KV partial (%s)" % {1: "simt", 2: "tcgen05 pair", 3: "tcgen05 cta_group::2 quad"}[dv.plan.kernel]},
         "alg_bytes": byts, "alg_flops": flops,
         "plan": dv.plan.as_dict(),
         "contiguous_us": contiguous_us,

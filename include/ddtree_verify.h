@@ -81,7 +81,8 @@ enum ddtree_status {
 /* Kernel variants of the split-KV partial stage. */
 #define DDTREE_KERNEL_AUTO 0
 #define DDTREE_KERNEL_SIMT 1         /* CUDA-core partial kernel              */
-#define DDTREE_KERNEL_TC   2         /* tcgen05 / TMEM partial kernel         */
+#define DDTREE_KERNEL_TC   2         /* tcgen05 / TMEM partial kernel, CTA pair per 128-row tile */
+#define DDTREE_KERNEL_TC2  3         /* tcgen05 cta_group::2 kernel, 4-CTA cluster per 256 rows  */
 
 /*
  * Execution plan: every size the launch needs, fixed on the host so the grid
@@ -100,13 +101,13 @@ typedef struct ddtree_plan {
   int32_t rows_per_req;     /* T*H query rows per request                     */
   int64_t pool_rows;        /* KV pool rows (index bound); <= 0: unchecked    */
   int32_t max_keys;         /* max_b (P_b + T) of the planned lengths         */
-  int32_t kernel;           /* DDTREE_KERNEL_SIMT or DDTREE_KERNEL_TC         */
+  int32_t kernel;           /* DDTREE_KERNEL_SIMT, _TC or _TC2                */
   int32_t tile_keys;        /* keys per inner tile                            */
   int32_t chunk_keys;       /* keys per split (multiple of tile_keys)         */
   int32_t total_splits;     /* sum_b ceil((P_b+T)/chunk_keys), planned        */
   int32_t row_tile;         /* query rows per work item                       */
   int32_t row_tiles;        /* ceil(rows_per_req / row_tile)                  */
-  int32_t num_sms;          /* SM count the plan was made for                 */
+  int32_t num_sms;          /* SMs the plan spreads its work items over       */
   int32_t q_latent_row_stride; /* elements between (t,h) rows; 0 -> 512       */
   int32_t q_rope_row_stride;   /* elements between (t,h) rows; 0 -> 64        */
   int64_t workspace_bytes;  /* bytes the workspace must hold                  */
@@ -120,7 +121,8 @@ typedef struct ddtree_plan {
  * heads with prefix lengths prefix_lens_host[0..batch) (host array).  The
  * plan is an upper bound: a later call may use shorter device lengths (e.g.
  * graph replay), never longer ones.  pool_rows bounds kv_indices (<= 0
- * disables the check).  Host-only apart from a cached SM-count query.
+ * disables the check).  Host-only apart from cached device queries (SM
+ * count, and how many clusters of the chosen kernel are resident at once).
  * Errors: DDTREE_EINVAL (sizes out of range, null pointers),
  * DDTREE_EUNSUPPORTED (no CUDA device to size for).
  */
@@ -128,8 +130,12 @@ DDTREE_API int ddtree_verify_mla_plan(int batch, int n_nodes, int n_heads,
                            const int32_t* prefix_lens_host, int64_t pool_rows,
                            ddtree_plan_t* plan);
 
-/* Same, for an explicit SM count and partial-kernel variant (no device
- * query; kernel = DDTREE_KERNEL_AUTO picks per shape).  Used to plan off-GPU. */
+/* Same, for an explicit SM count and partial-kernel variant
+ * (kernel = DDTREE_KERNEL_AUTO picks per shape).  num_sms >= 1 makes it a
+ * pure host computation (used to plan off-GPU); num_sms = 0 asks the current
+ * device, as ddtree_verify_mla_plan does: the SMs the chosen kernel's
+ * clusters can occupy at once, which is below the SM count when a GPC's SMs
+ * do not divide into whole clusters. */
 DDTREE_API int ddtree_verify_mla_plan_ex(int batch, int n_nodes, int n_heads,
                               const int32_t* prefix_lens_host, int64_t pool_rows,
                               int num_sms, int kernel, ddtree_plan_t* plan);

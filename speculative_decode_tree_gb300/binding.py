@@ -32,6 +32,7 @@ DDTREE_ST_TIMEOUT = 0x8
 DDTREE_KERNEL_AUTO = 0
 DDTREE_KERNEL_SIMT = 1
 DDTREE_KERNEL_TC = 2
+DDTREE_KERNEL_TC2 = 3
 
 EXPORTS = (
     "ddtree_verify_mla_plan", "ddtree_verify_mla_plan_ex", "ddtree_verify_mla_workspace_size",

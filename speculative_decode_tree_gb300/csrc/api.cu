@@ -63,7 +63,7 @@ struct Geometry {
   int row_tile, tile_keys, waves;
 };
 Geometry geometry(int kernel) {
-  if (kernel == DDTREE_KERNEL_TC) return Geometry{128, 128, 1};
+  if (kernel == DDTREE_KERNEL_TC || kernel == DDTREE_KERNEL_TC2) return Geometry{128, 128, 1};
   return Geometry{32, 32, 4};
 }
 
@@ -72,6 +72,29 @@ Geometry geometry(int kernel) {
 int choose_kernel(int kernel, int rows_per_req, int64_t total_keys) {
   if (kernel != DDTREE_KERNEL_AUTO) return kernel;
   return ((int64_t)rows_per_req * total_keys >= 128 * 1024) ? DDTREE_KERNEL_TC : DDTREE_KERNEL_SIMT;
+}
+
+// SMs the chosen kernel can keep busy at once on the current device.  A
+// tensor-core work item is a cluster, and clusters are placed within one GPC,
+// so a GPC whose SM count is not a multiple of the cluster size leaves SMs
+// idle: the count is (clusters resident at once) x (cluster size).
+int usable_sms(int kernel, int* out) {
+  DevInfo info;
+  int rc = current_device_info(&info);
+  if (rc != DDTREE_OK) return rc;
+  if (kernel == DDTREE_KERNEL_SIMT || info.major != 10 || info.minor != 3) {
+    *out = info.sms;
+    return DDTREE_OK;
+  }
+  const int csize = kernel == DDTREE_KERNEL_TC2 ? 4 : 2;
+  int clusters = 0;
+  cudaError_t e = kernel == DDTREE_KERNEL_TC2 ? cluster_capacity_tc2(&clusters) : cluster_capacity_tc(&clusters);
+  if (e != cudaSuccess || clusters < 1) {
+    cudaGetLastError();
+    return DDTREE_EUNSUPPORTED;
+  }
+  *out = std::min(info.sms, clusters * csize);
+  return DDTREE_OK;
 }
 
 }  // namespace
@@ -86,8 +109,8 @@ extern "C" int ddtree_verify_mla_plan_ex(int batch, int n_nodes, int n_heads,
   if (batch < 1 || batch > DDTREE_MAX_BATCH) return DDTREE_EINVAL;
   if (n_nodes < 1 || n_nodes > DDTREE_MAX_NODES) return DDTREE_EINVAL;
   if (n_heads < 1 || n_heads > DDTREE_MAX_HEADS) return DDTREE_EINVAL;
-  if (num_sms < 1 || num_sms > 4096) return DDTREE_EINVAL;
-  if (kernel < DDTREE_KERNEL_AUTO || kernel > DDTREE_KERNEL_TC) return DDTREE_EINVAL;
+  if (num_sms < 0 || num_sms > 4096) return DDTREE_EINVAL;
+  if (kernel < DDTREE_KERNEL_AUTO || kernel > DDTREE_KERNEL_TC2) return DDTREE_EINVAL;
   int64_t total_keys = 0, max_keys = 0;
   for (int b = 0; b < batch; ++b) {
     if (prefix_lens_host[b] < 0 || prefix_lens_host[b] > (1 << 30)) return DDTREE_EINVAL;
@@ -105,8 +128,12 @@ extern "C" int ddtree_verify_mla_plan_ex(int batch, int n_nodes, int n_heads,
   p.rows_per_req = n_nodes * n_heads;
   p.pool_rows = pool_rows;
   p.max_keys = (int32_t)max_keys;
-  p.num_sms = num_sms;
   p.kernel = choose_kernel(kernel, p.rows_per_req, total_keys);
+  if (num_sms == 0) {
+    int rc = usable_sms(p.kernel, &num_sms);
+    if (rc != DDTREE_OK) return rc;
+  }
+  p.num_sms = num_sms;
   Geometry g = geometry(p.kernel);
   p.row_tile = g.row_tile;
   p.tile_keys = g.tile_keys;
@@ -115,8 +142,11 @@ extern "C" int ddtree_verify_mla_plan_ex(int batch, int n_nodes, int n_heads,
   // Split rule: enough work items (row tile x key chunk) for `waves` CTAs
   // per SM, with chunks a whole number of tiles.  A tensor-core work item is
   // a cluster of two CTAs (scorer + accumulator), so it occupies two SMs.
-  int64_t target_items = (int64_t)g.waves * num_sms / (p.kernel == DDTREE_KERNEL_TC ? 2 : 1);
-  int64_t target_splits = std::max<int64_t>(1, (target_items + p.row_tiles - 1) / p.row_tiles);
+  // The pair form is a cluster of four CTAs covering two row tiles.
+  const int64_t ctas_per_item = p.kernel == DDTREE_KERNEL_TC2 ? 4 : (p.kernel == DDTREE_KERNEL_TC ? 2 : 1);
+  const int64_t row_groups = p.kernel == DDTREE_KERNEL_TC2 ? (p.row_tiles + 1) / 2 : p.row_tiles;
+  int64_t target_items = (int64_t)g.waves * num_sms / ctas_per_item;
+  int64_t target_splits = std::max<int64_t>(1, (target_items + row_groups - 1) / row_groups);
   int64_t chunk = (total_keys + target_splits - 1) / target_splits;
   chunk = round_up(std::max<int64_t>(chunk, g.tile_keys), g.tile_keys);
   chunk = std::min<int64_t>(chunk, round_up(max_keys, g.tile_keys));
@@ -142,10 +172,7 @@ extern "C" int ddtree_verify_mla_plan_ex(int batch, int n_nodes, int n_heads,
 extern "C" int ddtree_verify_mla_plan(int batch, int n_nodes, int n_heads,
                                       const int32_t* prefix_lens_host, int64_t pool_rows,
                                       ddtree_plan_t* plan) {
-  DevInfo info;
-  int rc = current_device_info(&info);
-  if (rc != DDTREE_OK) return rc;
-  return ddtree_verify_mla_plan_ex(batch, n_nodes, n_heads, prefix_lens_host, pool_rows, info.sms,
+  return ddtree_verify_mla_plan_ex(batch, n_nodes, n_heads, prefix_lens_host, pool_rows, 0,
                                    DDTREE_KERNEL_AUTO, plan);
 }
 
@@ -161,7 +188,8 @@ int validate_plan(const ddtree_plan_t* p) {
       p->n_nodes > DDTREE_MAX_NODES || p->n_heads < 1 || p->n_heads > DDTREE_MAX_HEADS)
     return DDTREE_EINVAL;
   if (p->rows_per_req != p->n_nodes * p->n_heads) return DDTREE_EINVAL;
-  if (p->kernel != DDTREE_KERNEL_SIMT && p->kernel != DDTREE_KERNEL_TC) return DDTREE_EINVAL;
+  if (p->kernel != DDTREE_KERNEL_SIMT && p->kernel != DDTREE_KERNEL_TC && p->kernel != DDTREE_KERNEL_TC2)
+    return DDTREE_EINVAL;
   Geometry g = geometry(p->kernel);
   if (p->row_tile != g.row_tile || p->tile_keys != g.tile_keys) return DDTREE_EINVAL;
   if (p->row_tiles != (p->rows_per_req + g.row_tile - 1) / g.row_tile) return DDTREE_EINVAL;
@@ -233,7 +261,9 @@ int run(const ddtree_plan_t* p, const uint16_t* q_latent, const uint16_t* q_rope
   cudaError_t e = cudaSuccess;
   if (ev && ev[0]) e = record_event(ev[0], stream);
   if (e == cudaSuccess)
-    e = (p->kernel == DDTREE_KERNEL_TC) ? launch_partial_tc(a, stream) : launch_partial_simt(a, stream);
+    e = (p->kernel == DDTREE_KERNEL_TC2)  ? launch_partial_tc2(a, stream)
+        : (p->kernel == DDTREE_KERNEL_TC) ? launch_partial_tc(a, stream)
+                                          : launch_partial_simt(a, stream);
   if (e == cudaSuccess && ev && ev[1]) e = record_event(ev[1], stream);
   if (e == cudaSuccess) e = launch_combine(a, stream);
   if (e == cudaSuccess && ev && ev[2]) e = record_event(ev[2], stream);

@@ -123,6 +123,9 @@ __device__ __forceinline__ float bf16_hi(uint32_t v) { return __uint_as_float(v 
 // ---- launchers (one per .cu file) ----
 cudaError_t launch_partial_simt(const VerifyArgs& a, cudaStream_t stream);
 cudaError_t launch_partial_tc(const VerifyArgs& a, cudaStream_t stream);
+cudaError_t launch_partial_tc2(const VerifyArgs& a, cudaStream_t stream);
+cudaError_t cluster_capacity_tc(int* clusters);
+cudaError_t cluster_capacity_tc2(int* clusters);
 cudaError_t launch_combine(const VerifyArgs& a, cudaStream_t stream);
 cudaError_t launch_ancestor_mask(const int32_t* parent, int batch, int n_nodes, uint64_t* anc,
                                  uint32_t* status, cudaStream_t stream);

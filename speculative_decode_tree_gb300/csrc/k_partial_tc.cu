@@ -30,6 +30,7 @@
 // DDTREE_ST_TIMEOUT, stops issuing work, waits (bounded) for its own
 // tensor-core work and frees its TMEM.
 #include <cuda.h>
+#include <string.h>
 
 #include "common.cuh"
 #include "tc_ptx.cuh"
@@ -42,7 +43,7 @@ using namespace ptx;
 constexpr int TK = 128;                 // keys per tile
 constexpr int ROWS = 128;               // query rows per work item
 constexpr int CHUNK = 16384;            // one 64-column chunk of a tile: 128 keys x 128 B
-constexpr int QRING = 8;                // scorer key-chunk slots
+constexpr int QRING = 10;               // scorer key-chunk slots
 constexpr int VRING = 4;                // accumulator slots, each a pair of chunks (32 KB)
 constexpr int PTILE = 32768;            // bf16 P tile: 2 swizzle atoms of 128 rows x 128 B
 constexpr int META = 1040;              // alpha[128], lfin[128], flag words[4]
@@ -55,15 +56,15 @@ constexpr uint64_t kWaitNs = 2000000000ull;
 // Shared-memory map (offsets from a 1024-aligned base).
 constexpr int Q_ROPE = 0;                               // scorer: 16 KB
 constexpr int Q_RING = Q_ROPE + CHUNK;                  // scorer: 8 x 16 KB
-constexpr int Q_STAGE = Q_RING + QRING * CHUNK;         // scorer: 2 x PBUF
-constexpr int Q_END = Q_STAGE + 2 * PBUF;
+constexpr int Q_STAGE = Q_RING + QRING * CHUNK;         // scorer: 1 x PBUF (P staging)
+constexpr int Q_END = Q_STAGE + PBUF;
 constexpr int V_PBUF = 0;                               // accumulator: 2 x PBUF
 constexpr int V_RING = V_PBUF + 2 * PBUF;               // accumulator: 4 x 32 KB
 constexpr int V_END = V_RING + VRING * 2 * CHUNK;
 constexpr int BIG_END = (Q_END > V_END ? Q_END : V_END);
 
 struct __align__(8) Ctrl {
-  uint64_t kfull[QRING], kempty[QRING];  // scorer ring
+  uint64_t kfull[QRING], kempty[QRING];  // scorer ring (QRING <= 16)
   uint64_t sfull[2], sempty[2];          // scorer S buffers
   uint64_t pfree[2];                     // scorer: peer released P buffer (2 arrivals)
   uint64_t vfull[VRING], vempty[VRING];  // accumulator ring
@@ -143,23 +144,27 @@ struct TileIdx {
   bool contiguous;
 };
 
-__device__ __forceinline__ TileIdx load_tile_indices(const VerifyArgs& a, const Item& it, int tile, int lane) {
-  const int k0 = it.k_begin + tile * TK + 4 * lane;
+// Raw index loads of one tile for this lane (no use of the values, so the
+// loads can be issued a tile early); finish_tile_indices validates them.
+struct RawIdx {
   int v[4];
+};
+__device__ __forceinline__ RawIdx raw_tile_indices(const VerifyArgs& a, const Item& it, int tile, int lane) {
+  const int k0 = it.k_begin + tile * TK + 4 * lane;
+  RawIdx r;
 #pragma unroll
-  for (int j = 0; j < 4; ++j) {
-    int id = -1;
-    if (k0 + j < it.k_end) {
-      id = __ldg(a.kv_indices + it.loc.idx_base + k0 + j);
-      if (id < 0 || (a.pool_rows > 0 && id >= a.pool_rows)) id = -1;
-    }
-    v[j] = id;
-  }
+  for (int j = 0; j < 4; ++j) r.v[j] = (k0 + j < it.k_end) ? __ldg(a.kv_indices + it.loc.idx_base + k0 + j) : -1;
+  return r;
+}
+__device__ __forceinline__ TileIdx finish_tile_indices(const VerifyArgs& a, RawIdx r, int lane) {
+#pragma unroll
+  for (int j = 0; j < 4; ++j)
+    if (r.v[j] < 0 || (a.pool_rows > 0 && r.v[j] >= a.pool_rows)) r.v[j] = -1;
   TileIdx t;
-  t.k4 = make_int4(v[0], v[1], v[2], v[3]);
-  t.first = __shfl_sync(0xffffffffu, v[0], 0);
-  const bool run = v[0] >= 0 && v[0] == t.first + 4 * lane && v[1] == v[0] + 1 && v[2] == v[0] + 2 &&
-                   v[3] == v[0] + 3;
+  t.k4 = make_int4(r.v[0], r.v[1], r.v[2], r.v[3]);
+  t.first = __shfl_sync(0xffffffffu, r.v[0], 0);
+  const bool run = r.v[0] >= 0 && r.v[0] == t.first + 4 * lane && r.v[1] == r.v[0] + 1 &&
+                   r.v[2] == r.v[0] + 2 && r.v[3] == r.v[0] + 3;
   t.contiguous = __all_sync(0xffffffffu, run);
   return t;
 }
@@ -262,8 +267,12 @@ __device__ void scorer(const VerifyArgs& a, const PoolMaps& maps, const Item& it
   if (prank >= 0) {
     // ---- producers: key chunks 0..8 of every tile
     int n = 0;
+    // Indices are loaded one tile ahead so their latency hides behind a
+    // tile's worth of copies.
+    RawIdx raw_next = raw_tile_indices(a, it, 0, lane);
     for (int t = 0; t < it.ntiles; ++t) {
-      const TileIdx ti = load_tile_indices(a, it, t, lane);
+      const TileIdx ti = finish_tile_indices(a, raw_next, lane);
+      if (t + 1 < it.ntiles) raw_next = raw_tile_indices(a, it, t + 1, lane);
       const MyKeys mk = my_keys(ti, lane, prank, kScorerProducers);
       for (int ch = 0; ch < 9; ++ch, ++n) {
         const int slot = n % QRING;
@@ -373,10 +382,11 @@ __device__ void scorer(const VerifyArgs& a, const PoolMaps& maps, const Item& it
         m_ref = mt;
       }
       const float nm = (m_ref == -INFINITY) ? 0.f : -m_ref;
-      // Staging buffer s is free once the copy of tile t-2 has read it.
-      if (r == 0) asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
+      // The staging buffer is free once the previous tile's copy has read it
+      // (long done by now: a whole QK^T tile passed since it was issued).
+      if (r == 0) asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
       named_bar(1, 128);
-      uint8_t* stg = sm + Q_STAGE + s * PBUF;
+      uint8_t* stg = sm + Q_STAGE;
       float ps[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
       for (int cc = 0; cc < 16; ++cc) {  // 16-byte chunk cc = keys 8cc .. 8cc+7
@@ -433,8 +443,10 @@ __device__ void accumulator(const VerifyArgs& a, const PoolMaps& maps, const Ite
   if (prank >= 0) {
     // ---- producers: value chunk pairs (0,1) .. (6,7) of every tile
     int n = 0;
+    RawIdx raw_next = raw_tile_indices(a, it, 0, lane);
     for (int t = 0; t < it.ntiles; ++t) {
-      const TileIdx ti = load_tile_indices(a, it, t, lane);
+      const TileIdx ti = finish_tile_indices(a, raw_next, lane);
+      if (t + 1 < it.ntiles) raw_next = raw_tile_indices(a, it, t + 1, lane);
       const MyKeys mk = my_keys(ti, lane, prank, kAccProducers);
       for (int q = 0; q < 4; ++q, ++n) {
         const int slot = n % VRING;
@@ -716,10 +728,10 @@ cudaError_t make_pool_maps(const VerifyArgs& a, PoolMaps* m) {
 
 }  // namespace
 
-cudaError_t launch_partial_tc(const VerifyArgs& a, cudaStream_t stream) {
-  PoolMaps maps;
-  cudaError_t me = make_pool_maps(a, &maps);
-  if (me != cudaSuccess) return me;
+namespace {
+// The kernel needs more than the default 48 KB of dynamic shared memory;
+// the attribute is set once per device.
+cudaError_t ensure_smem_attr() {
   static bool attr_set[64] = {};
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -729,9 +741,32 @@ cudaError_t launch_partial_tc(const VerifyArgs& a, cudaStream_t stream) {
     if (e != cudaSuccess) return e;
     if (dev >= 0 && dev < 64) attr_set[dev] = true;
   }
+  return cudaSuccess;
+}
+}  // namespace
+
+cudaError_t launch_partial_tc(const VerifyArgs& a, cudaStream_t stream) {
+  PoolMaps maps;
+  cudaError_t e = make_pool_maps(a, &maps);
+  if (e != cudaSuccess) return e;
+  e = ensure_smem_attr();
+  if (e != cudaSuccess) return e;
   dim3 grid(2 * a.row_tiles * a.total_splits);
   partial_tc_kernel<<<grid, kThreads, kSmemBytes, stream>>>(a, maps);
   return cudaGetLastError();
+}
+
+// How many 2-CTA clusters of this kernel the current device runs at
+// once.  Clusters are placed within one GPC, so this can be below SMs / 2.
+cudaError_t cluster_capacity_tc(int* clusters) {
+  cudaError_t e = ensure_smem_attr();
+  if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg;
+  memset(&cfg, 0, sizeof(cfg));
+  cfg.gridDim = dim3(2 * 64);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = kSmemBytes;
+  return cudaOccupancyMaxActiveClusters(clusters, (void*)partial_tc_kernel, &cfg);
 }
 
 }  // namespace ddtree

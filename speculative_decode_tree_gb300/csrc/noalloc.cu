@@ -150,7 +150,9 @@ extern "C" int ddtree_verify_mla_noalloc(const ddtree_bf16_t* q_latent, const dd
     cudaGetLastError();
     return DDTREE_ECUDA;
   }
-  cudaError_t e = (plan.kernel == DDTREE_KERNEL_TC) ? launch_partial_tc(a, s) : launch_partial_simt(a, s);
+  cudaError_t e = (plan.kernel == DDTREE_KERNEL_TC2)  ? launch_partial_tc2(a, s)
+                  : (plan.kernel == DDTREE_KERNEL_TC) ? launch_partial_tc(a, s)
+                                                      : launch_partial_simt(a, s);
   if (e == cudaSuccess) e = launch_combine(a, s);
   if (e != cudaSuccess) {
     cudaGetLastError();

@@ -33,9 +33,8 @@ class DeviceVerify:
             self.plan = B.ddtree_verify_mla_plan(inp.batch, inp.n_nodes, inp.n_heads,
                                                  inp.prefix_lens.tolist(), pool_rows)
         else:
-            sms = torch.cuda.get_device_properties(dev).multi_processor_count
             self.plan = B.ddtree_verify_mla_plan_ex(inp.batch, inp.n_nodes, inp.n_heads,
-                                                    inp.prefix_lens.tolist(), pool_rows, sms, kernel)
+                                                    inp.prefix_lens.tolist(), pool_rows, 0, kernel)
         rows = inp.batch * inp.n_nodes
         self.out = torch.empty(rows, inp.n_heads, 512, dtype=torch.bfloat16, device=dev)
         self.lse = torch.empty(rows, inp.n_heads, dtype=torch.float32, device=dev)

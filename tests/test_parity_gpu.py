@@ -14,7 +14,7 @@ from parity_util import assert_within_tolerance, cached_workload, oracle_rows
 
 pytestmark = pytest.mark.gpu
 
-KERNELS = [B.DDTREE_KERNEL_SIMT, B.DDTREE_KERNEL_TC]
+KERNELS = [B.DDTREE_KERNEL_SIMT, B.DDTREE_KERNEL_TC, B.DDTREE_KERNEL_TC2]
 
 
 def _compare_all(inp, kernel=None, what=""):
