@@ -24,6 +24,7 @@ import math
 import os
 import statistics
 import subprocess
+import threading
 import sys
 import time
 
@@ -88,57 +89,108 @@ def _peaks():
 
 
 class ClockSampler:
-    """nvidia-smi clock / throttle-reason samples while the timed region runs."""
+    """SM clock and clock-event (throttle) reasons sampled while the timed region runs.
 
-    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
-              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
-              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    Reads NVML through ctypes every 2 ms (read-only queries; nothing is set),
+    so even a region of a few milliseconds gets samples; falls back to
+    `nvidia-smi -lms 100` when NVML cannot be loaded."""
+
+    REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
+               0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown"}
 
     def __init__(self, device_index: int):
-        self.proc = None
         self.idx = device_index
-        self.out = os.path.join("/tmp", f"ddtree_clocks_{os.getpid()}.csv")
+        self.samples = []
+        self.max_mhz = None
+        self.stop = threading.Event()
+        self.thread = None
+        self.nvml = None
+        self.handle = None
+        self.smi = None
+        try:
+            import ctypes
+            nv = ctypes.CDLL("libnvidia-ml.so.1")
+            if nv.nvmlInit_v2() != 0:
+                raise RuntimeError("nvmlInit failed")
+            h = ctypes.c_void_p()
+            props = torch.cuda.get_device_properties(device_index)
+            bus = getattr(props, "pci_bus_id", None)
+            ok = False
+            if bus is not None:
+                pci = "%08x:%02x:%02x.0" % (getattr(props, "pci_domain_id", 0), bus, getattr(props, "pci_device_id", 0))
+                ok = nv.nvmlDeviceGetHandleByPciBusId_v2(pci.encode(), ctypes.byref(h)) == 0
+            if not ok and nv.nvmlDeviceGetHandleByIndex_v2(ctypes.c_uint(device_index), ctypes.byref(h)) != 0:
+                raise RuntimeError("no NVML handle")
+            mx = ctypes.c_uint()
+            if nv.nvmlDeviceGetMaxClockInfo(h, ctypes.c_int(1), ctypes.byref(mx)) == 0:
+                self.max_mhz = float(mx.value)
+            self.reason_fn = getattr(nv, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+                nv.nvmlDeviceGetCurrentClocksThrottleReasons
+            self.nvml, self.handle, self.ct = nv, h, ctypes
+        except Exception:
+            self.nvml = None
+
+    def sample(self):
+        """One NVML sample (also called between timed steps by the caller)."""
+        if self.nvml is None:
+            return
+        ct, nv, h = self.ct, self.nvml, self.handle
+        clk, rs = ct.c_uint(), ct.c_ulonglong()
+        if nv.nvmlDeviceGetClockInfo(h, ct.c_int(1), ct.byref(clk)) == 0:
+            r = rs.value if self.reason_fn(h, ct.byref(rs)) == 0 else 0
+            self.samples.append((float(clk.value), int(r)))
+
+    def _loop(self):
+        while not self.stop.is_set():
+            self.sample()
+            time.sleep(0.002)
 
     def __enter__(self):
-        try:
-            self.f = open(self.out, "w")
-            self.proc = subprocess.Popen(
-                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
-                 "-i", str(self.idx), "-lms", "100"], stdout=self.f, stderr=subprocess.DEVNULL)
-        except Exception:
-            self.proc = None
+        if self.nvml is not None:
+            self.thread = threading.Thread(target=self._loop, daemon=True)
+            self.thread.start()
+        else:
+            try:
+                self.smi_out = os.path.join("/tmp", f"ddtree_clocks_{os.getpid()}.csv")
+                self.f = open(self.smi_out, "w")
+                self.smi = subprocess.Popen(
+                    ["nvidia-smi", "--query-gpu=clocks.sm,clocks.max.sm,clocks_event_reasons.active",
+                     "--format=csv,noheader,nounits", "-i", str(self.idx), "-lms", "100"],
+                    stdout=self.f, stderr=subprocess.DEVNULL)
+            except Exception:
+                self.smi = None
         return self
 
     def __exit__(self, *exc):
-        if self.proc is not None:
-            self.proc.terminate()
+        if self.thread is not None:
+            self.stop.set()
+            self.thread.join(timeout=5)
+        if self.smi is not None:
+            self.smi.terminate()
             try:
-                self.proc.wait(timeout=5)
+                self.smi.wait(timeout=5)
             except Exception:
-                self.proc.kill()
+                self.smi.kill()
             self.f.close()
+            for line in open(self.smi_out):
+                parts = [p.strip() for p in line.split(",")]
+                try:
+                    self.samples.append((float(parts[0]), int(parts[2], 16)))
+                    self.max_mhz = max(self.max_mhz or 0.0, float(parts[1]))
+                except (ValueError, IndexError):
+                    continue
 
     def summary(self):
-        if self.proc is None or not os.path.exists(self.out):
+        if not self.samples:
             return None
-        sm, mx, reasons = [], [], set()
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for line in open(self.out):
-            parts = [p.strip() for p in line.split(",")]
-            if len(parts) < 9:
-                continue
-            try:
-                sm.append(float(parts[1]))
-                mx.append(float(parts[2]))
-            except ValueError:
-                continue
-            for n, v in zip(names, parts[5:9]):
-                if v.lower().startswith("active"):
-                    reasons.add(n)
-        if not sm:
-            return None
-        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
-                "samples": len(sm)}
+        reasons = set()
+        for _, r in self.samples:
+            for bit, name in self.REASONS.items():
+                if r & bit:
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(m for m, _ in self.samples), "sm_max_mhz": self.max_mhz,
+                "reasons": sorted(reasons), "samples": len(self.samples),
+                "source": "nvml" if self.nvml is not None else "nvidia-smi"}
 
 
 def _pct(xs, q):
@@ -213,8 +265,13 @@ def run_ours(args, world, rank, local):
     with torch.cuda.stream(stream):
         dv.run_timed(stage)  # first call outside capture (kernel attributes)
     stream.synchronize()
+    # The timed graph is the plain call; a second graph with event records
+    # between the two kernels gives the per-kernel split, timed separately.
     graph = torch.cuda.CUDAGraph()
     with torch.cuda.graph(graph, stream=stream):
+        dv.run()
+    graph_split = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph_split, stream=stream):
         dv.run_timed(stage)
 
     def one_step():
@@ -224,25 +281,32 @@ def run_ours(args, world, rank, local):
             graph.replay()
             t1.record(stream)
         stream.synchronize()
-        return t0.elapsed_time(t1) * 1e3, stage[0].elapsed_time(stage[1]) * 1e3, \
-            stage[1].elapsed_time(stage[2]) * 1e3
+        return t0.elapsed_time(t1) * 1e3
 
     for _ in range(args.warmup):
         one_step()
     _barrier(world)
     torch.cuda.synchronize()
-    calls, partials, combines = [], [], []
+    calls = []
     with ClockSampler(local) as clk:
         wall0 = time.perf_counter()
         for _ in range(args.steps):
-            c, p, m = one_step()
-            calls.append(c)
-            partials.append(p)
-            combines.append(m)
+            calls.append(one_step())
+            clk.sample()
         torch.cuda.synchronize()
         _barrier(world)
         wall = time.perf_counter() - wall0
     status = dv.status(stream)
+
+    partials, combines = [], []
+    for i in range(args.warmup + args.steps):
+        with torch.cuda.stream(stream):
+            flush.zero_()
+            graph_split.replay()
+        stream.synchronize()
+        if i >= args.warmup:
+            partials.append(stage[0].elapsed_time(stage[1]) * 1e3)
+            combines.append(stage[1].elapsed_time(stage[2]) * 1e3)
 
     call_us = _max_over_ranks(world, statistics.median(calls))
     mean_call_us = _max_over_ranks(world, statistics.mean(calls))

@@ -67,11 +67,14 @@ Geometry geometry(int kernel) {
   return Geometry{32, 32, 4};
 }
 
-// The tensor-core kernel works on 128-row tiles of 128 keys; below about one
-// such tile's worth of (row, key) pairs the CUDA-core kernel is used.
+// The tensor-core kernels work on 128-row tiles of 128 keys; below about one
+// such tile's worth of (row, key) pairs the CUDA-core kernel is used.  With
+// two or more row tiles per request the cluster-of-four kernel, which gathers
+// each key tile once per pair of row tiles, takes over from the pair kernel.
 int choose_kernel(int kernel, int rows_per_req, int64_t total_keys) {
   if (kernel != DDTREE_KERNEL_AUTO) return kernel;
-  return ((int64_t)rows_per_req * total_keys >= 128 * 1024) ? DDTREE_KERNEL_TC : DDTREE_KERNEL_SIMT;
+  if ((int64_t)rows_per_req * total_keys < 128 * 1024) return DDTREE_KERNEL_SIMT;
+  return rows_per_req > 128 ? DDTREE_KERNEL_TC2 : DDTREE_KERNEL_TC;
 }
 
 // SMs the chosen kernel can keep busy at once on the current device.  A

@@ -50,8 +50,15 @@ constexpr int ROWS = 128;                // query rows per CTA
 constexpr int HALF = 64;                 // keys per scorer CTA per tile
 constexpr int SCHUNK = HALF * 128;       // scorer chunk: 64 keys x 64 columns (8 KB)
 constexpr int VCHUNK = TK * 128;         // accumulator chunk: 128 keys x 64 columns (16 KB)
-constexpr int QRING = 20;                // scorer chunk slots (2.2 tiles)
-constexpr int VRING = 8;                 // accumulator chunk slots (2 tiles)
+// The key rings are rings of units of several chunks with one mbarrier per
+// unit: a producer warp signals a unit with one cp.async-tracked arrive, which
+// keeps more bytes in flight per arrive than a barrier per chunk.
+constexpr int QU = 3;                    // scorer chunks per unit (24 KB)
+constexpr int QUNITS = 6;                // scorer unit slots (2 tiles)
+constexpr int QUNIT_BYTES = QU * SCHUNK;
+constexpr int VU = 2;                    // accumulator chunks per unit (32 KB)
+constexpr int VUNITS = 4;                // accumulator unit slots (2 tiles)
+constexpr int VUNIT_BYTES = VU * VCHUNK;
 constexpr int PTILE = 32768;             // bf16 P tile: 2 swizzle atoms of 128 rows x 128 B
 constexpr int META = 1040;               // alpha[128], lfin[128], flag words[4]
 constexpr int PCOPY = PTILE + META;      // bytes shipped per tile (multiple of 16)
@@ -59,29 +66,32 @@ constexpr int PBUF = 34816;              // P buffer stride (1024-aligned)
 constexpr int kThreads = 384;            // 12 warps
 constexpr int kScorerProducers = 7;      // warps 0, 2, 3, 8..11
 constexpr int kAccProducers = 6;         // warps 0, 3, 8..11
+constexpr int kScorerLsuChunks = 6;      // scorer chunks 0..5 by cp.async, 6..8 by TMA gather4
+constexpr int kAccLsuChunks = 3;         // accumulator chunks q = 0..2 by cp.async, q = 3 by TMA gather4
 constexpr float kLazyRescale = 8.0f;     // rescale only when the max grows by > 2^8 (log2 units)
 constexpr uint64_t kWaitNs = 2000000000ull;
 constexpr uint16_t kScorerPair = 0x3, kAccPair = 0xC;
 
 // Shared-memory map (offsets from a 1024-aligned base).
 constexpr int Q_ROPE = 0;                          // scorer: 16 KB
-constexpr int Q_RING = Q_ROPE + VCHUNK;            // scorer: 20 x 8 KB
-constexpr int Q_STAGE = Q_RING + QRING * SCHUNK;   // scorer: P staging
+constexpr int Q_RING = Q_ROPE + VCHUNK;            // scorer: 6 x 24 KB
+constexpr int Q_STAGE = Q_RING + QUNITS * QUNIT_BYTES;  // scorer: P staging
 constexpr int Q_END = Q_STAGE + PBUF;
 constexpr int V_PBUF = 0;                          // accumulator: 2 x PBUF
 constexpr int V_RING = V_PBUF + 2 * PBUF;          // accumulator: 8 x 16 KB
-constexpr int V_END = V_RING + VRING * VCHUNK;
+constexpr int V_END = V_RING + VUNITS * VUNIT_BYTES;
 constexpr int BIG_END = (Q_END > V_END ? Q_END : V_END);
 
 struct __align__(8) Ctrl {
   // scorer
-  uint64_t kfull[QRING], kpeer[QRING], kempty[QRING];
+  uint64_t kfull[QUNITS], kpeer[QUNITS], kempty[QUNITS];
   uint64_t sfull[2], sempty[2], pfree[2];
   // accumulator
-  uint64_t vfull[VRING], vpeer[VRING], vempty[VRING];
+  uint64_t vfull[VUNITS], vpeer[VUNITS], vempty[VUNITS];
   uint64_t pfull[2], ppeer[2], pvdone[2], corr_done[2];
   // both
   uint64_t mma_done;
+  uint64_t q_ready;   // scorer: Q latent in TMEM and Q rope in shared memory
   uint32_t tmem_base;
   uint32_t abort;
   uint32_t key_mask[2][4];
@@ -159,6 +169,8 @@ struct Item {
 struct PoolMaps {
   CUtensorMap half;   // 64 columns x 64 rows box: a scorer's half of a contiguous tile
   CUtensorMap tile;   // 64 columns x 128 rows box: an accumulator chunk of a contiguous tile
+  CUtensorMap po;     // partial O [splits][rows_per_req][512] fp32, 32 columns x 128 rows box
+  CUtensorMap row;    // 64 columns x 1 row box: four scattered rows per gather4 load
 };
 
 // One tile's 128 indices: lane l holds keys 4l .. 4l+3 (-1 past the chunk or
@@ -191,37 +203,44 @@ __device__ __forceinline__ TileIdx finish_tile_indices(const VerifyArgs& a, RawI
   return t;
 }
 
-// Index of key (4 g + lane/8) of the groups this producer lane copies:
-// groups g = rank, rank + np, ... < ngroups, taken from the lane that holds
-// them (tile key 4 (g0 + g) + lane/8, g0 = first group of this CTA's keys).
+// Index of key (4 g + lane/8) of the groups this producer lane copies: a
+// contiguous block of groups g = first .. first+n-1 (of ngroups, split as
+// evenly as the np producer warps allow), taken from the lane that holds them
+// (tile key 4 (g0 + g) + lane/8, g0 = first group of this CTA's keys).
 struct MyKeys {
   int id[6];
   int n;
+  int first;
 };
 __device__ __forceinline__ MyKeys my_keys(const TileIdx& ti, int lane, int rank, int np, int g0, int ngroups) {
   MyKeys mk;
-  mk.n = 0;
+  const int per = ngroups / np, extra = ngroups % np;
+  mk.first = rank * per + min(rank, extra);
+  mk.n = per + (rank < extra ? 1 : 0);
   const int sel = lane >> 3;
 #pragma unroll
   for (int j = 0; j < 6; ++j) {
-    const int g = rank + j * np;
+    const int g = mk.first + j;
     const int src = (g0 + g) & 31;
     const int x = __shfl_sync(0xffffffffu, ti.k4.x, src);
     const int y = __shfl_sync(0xffffffffu, ti.k4.y, src);
     const int z = __shfl_sync(0xffffffffu, ti.k4.z, src);
     const int w = __shfl_sync(0xffffffffu, ti.k4.w, src);
     mk.id[j] = sel == 0 ? x : sel == 1 ? y : sel == 2 ? z : w;
-    if (g < ngroups) mk.n = j + 1;
   }
   return mk;
 }
 
 // Fills one 64-column chunk (columns 64*col_chunk ..) of `nkeys` key rows
 // (tile keys key0 .. key0+nkeys-1) into `dst` (row k at dst + 128 k,
-// 128-byte swizzled) and arrives on `bar` once per lane.
+// 128-byte swizzled).  TMA bytes are expected on `bar`; the caller arrives
+// on it once per lane after the last chunk of a unit.  Scattered rows come
+// by 16-byte cp.async (load/store unit) or, when `g4` is set, by TMA gather4
+// loads of four rows each: the TMA engine is a second path into shared
+// memory, so giving it some of the chunks raises a CTA's gather rate.
 __device__ __forceinline__ void fill_chunk(const PoolMaps& maps, const uint16_t* pool, uint8_t* dst, int col_chunk,
                                            int key0, int nkeys, const TileIdx& ti, const MyKeys& mk, int rank,
-                                           int np, int lane, uint64_t* bar) {
+                                           int lane, uint64_t* bar, bool g4) {
   if (ti.contiguous) {
     if (rank == 0 && lane == 0) {
       mbar_expect_tx(bar, nkeys * 128);
@@ -232,20 +251,39 @@ __device__ __forceinline__ void fill_chunk(const PoolMaps& maps, const uint16_t*
           : "memory");
     }
     __syncwarp();
+  } else if (g4) {
+    if (lane == 0 && mk.n > 0) mbar_expect_tx(bar, mk.n * 512);
+#pragma unroll
+    for (int j = 0; j < 6; ++j) {
+      if (j < mk.n) {  // warp-uniform
+        // Rows of group first+j are held by lanes 0, 8, 16, 24; a missing
+        // key (-1) reads row 0 instead: its score is masked and its weight is 0.
+        const int r0 = max(mk.id[j], 0);
+        const int r1 = max(__shfl_sync(0xffffffffu, mk.id[j], 8), 0);
+        const int r2 = max(__shfl_sync(0xffffffffu, mk.id[j], 16), 0);
+        const int r3 = max(__shfl_sync(0xffffffffu, mk.id[j], 24), 0);
+        if (lane == 0)
+          asm volatile(
+              "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes"
+              " [%0], [%1, {%2, %3, %4, %5, %6}], [%7];" ::"r"(smem_u32(dst + 4 * (mk.first + j) * 128)),
+              "l"(&maps.row), "r"(col_chunk * 64), "r"(r0), "r"(r1), "r"(r2), "r"(r3), "r"(smem_u32(bar))
+              : "memory");
+      }
+    }
+    __syncwarp();
   } else {
     const int piece = lane & 7;
     const uint32_t base = smem_u32(dst);
 #pragma unroll
     for (int j = 0; j < 6; ++j) {
       if (j < mk.n) {
-        const int row = 4 * (rank + j * np) + (lane >> 3);  // row within this chunk
+        const int row = 4 * (mk.first + j) + (lane >> 3);  // row within this chunk
         const int id = mk.id[j];
         const uint16_t* src = pool + (size_t)(id < 0 ? 0 : id) * kRow + col_chunk * 64 + piece * 8;
         cp_async16_zfill(base + row * 128 + ((piece ^ (row & 7)) << 4), src, id < 0 ? 0u : 16u);
       }
     }
   }
-  cp_async_mbar_arrive(bar);
 }
 
 // Pulls whole 1152-byte key rows of a tile into L2 (one bulk prefetch per
@@ -292,16 +330,19 @@ __device__ void scorer(const VerifyArgs& a, const PoolMaps& maps, const Item& it
       const TileIdx ti = finish_tile_indices(a, raw_next, lane);
       if (t + 1 < it.ntiles) raw_next = raw_tile_indices(a, it, t + 1, lane);
       const MyKeys mk = my_keys(ti, lane, prank, kScorerProducers, 16 * half, 16);
-      for (int ch = 0; ch < 9; ++ch, ++n) {
-        const int slot = n % QRING;
+      for (int u = 0; u < 9 / QU; ++u, ++n) {
+        const int slot = n % QUNITS;
         bool ok = true;
-        if (lane == 0) ok = wait_clu(&c->kempty[slot], ((n / QRING) & 1) ^ 1, c, a.status);
+        if (lane == 0) ok = wait_clu(&c->kempty[slot], ((n / QUNITS) & 1) ^ 1, c, a.status);
         if (!__shfl_sync(0xffffffffu, ok, 0)) {
           asm volatile("cp.async.wait_all;" ::: "memory");
           return;
         }
-        fill_chunk(maps, a.kv_pool, sm + Q_RING + slot * SCHUNK, ch, HALF * half, HALF, ti, mk, prank,
-                   kScorerProducers, lane, &c->kfull[slot]);
+#pragma unroll 1
+        for (int cc = 0; cc < QU; ++cc)
+          fill_chunk(maps, a.kv_pool, sm + Q_RING + slot * QUNIT_BYTES + cc * SCHUNK, QU * u + cc, HALF * half, HALF,
+                     ti, mk, prank, lane, &c->kfull[slot], QU * u + cc >= kScorerLsuChunks);
+        cp_async_mbar_arrive(&c->kfull[slot]);
       }
     }
     asm volatile("cp.async.wait_all;" ::: "memory");
@@ -311,28 +352,33 @@ __device__ void scorer(const VerifyArgs& a, const PoolMaps& maps, const Item& it
       constexpr uint32_t idesc = idesc_bf16_f32(256, 128, false, false);
       const uint64_t rope_desc = desc_sw128(smem_u32(sm + Q_ROPE), 16, 1024);
       int n = 0;
-      bool ok = true;
+      bool ok = wait_clu(&c->q_ready, 0, c, a.status);
+      tc_fence_after();
       for (int t = 0; t < it.ntiles && ok; ++t) {
         const int s = t & 1;
         const uint32_t sbuf = tmem + 256 + 128 * s;
         if (!wait_clu(&c->sempty[s], ((t >> 1) & 1) ^ 1, c, a.status)) { ok = false; break; }
         tc_fence_after();
-        for (int ch = 0; ch < 9; ++ch, ++n) {
-          const int slot = n % QRING;
-          const uint32_t ph = (n / QRING) & 1;
+        for (int u = 0; u < 9 / QU; ++u, ++n) {
+          const int slot = n % QUNITS;
+          const uint32_t ph = (n / QUNITS) & 1;
           if (!wait_clu(&c->kfull[slot], ph, c, a.status) || !wait_clu(&c->kpeer[slot], ph, c, a.status)) {
             ok = false;
             break;
           }
           fence_async_smem();  // cp.async (generic proxy) data -> tensor-core reads
           tc_fence_after();
-          const uint64_t kdesc = desc_sw128(smem_u32(sm + Q_RING + slot * SCHUNK), 16, 1024);
 #pragma unroll
-          for (int kk = 0; kk < 4; ++kk) {
-            const int ks = ch * 4 + kk;
-            const uint64_t bd = kdesc + (uint64_t)((kk * 32) >> 4);
-            if (ch < 8) mma2_ts(sbuf, tmem + ks * 8, bd, idesc, ks > 0);
-            else mma2_ss(sbuf, rope_desc + (uint64_t)((kk * 32) >> 4), bd, idesc, 1);
+          for (int cc = 0; cc < QU; ++cc) {
+            const int ch = QU * u + cc;
+            const uint64_t kdesc = desc_sw128(smem_u32(sm + Q_RING + slot * QUNIT_BYTES + cc * SCHUNK), 16, 1024);
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk) {
+              const int ks = ch * 4 + kk;
+              const uint64_t bd = kdesc + (uint64_t)((kk * 32) >> 4);
+              if (ch < 8) mma2_ts(sbuf, tmem + ks * 8, bd, idesc, ks > 0);
+              else mma2_ss(sbuf, rope_desc + (uint64_t)((kk * 32) >> 4), bd, idesc, 1);
+            }
           }
           commit2(&c->kempty[slot], kScorerPair);
         }
@@ -340,13 +386,16 @@ __device__ void scorer(const VerifyArgs& a, const PoolMaps& maps, const Item& it
       }
       commit2(&c->mma_done, kScorerPair);
     } else {
-      // ---- follower: forward "my half of chunk n landed" to the leader
+      // ---- follower: forward "my half of unit n landed" to the leader
       const uint32_t lead_kpeer = map_cluster(smem_u32(&c->kpeer[0]), rank - 1);
+      // The leader's MMAs read this CTA's Q too: it must be in place before
+      // the first forward.
+      if (!wait_clu(&c->q_ready, 0, c, a.status)) return;
       int n = 0;
       for (int t = 0; t < it.ntiles; ++t) {
-        for (int ch = 0; ch < 9; ++ch, ++n) {
-          const int slot = n % QRING;
-          if (!wait_clu(&c->kfull[slot], (n / QRING) & 1, c, a.status)) return;
+        for (int u = 0; u < 9 / QU; ++u, ++n) {
+          const int slot = n % QUNITS;
+          if (!wait_clu(&c->kfull[slot], (n / QUNITS) & 1, c, a.status)) return;
           fence_async_smem();
           remote_arrive(lead_kpeer + slot * 8);
         }
@@ -358,6 +407,42 @@ __device__ void scorer(const VerifyArgs& a, const PoolMaps& maps, const Item& it
     const int w = warp - 4;
     const int req_row = it.row0 + r;
     const bool row_ok = req_row < a.rows_per_req;
+    {
+      // First, this row of Q into place while the producers already gather
+      // keys: latent -> TMEM lane r as packed bf16 pairs, rope -> shared
+      // memory (K-major, 128-byte swizzle).  16 loads in flight per thread.
+      const size_t g = (size_t)it.loc.b * a.rows_per_req + (row_ok ? req_row : 0);
+      const uint4* ql = reinterpret_cast<const uint4*>(a.q_latent + g * a.q_lat_stride);
+      const uint32_t lane_addr = tmem + ((uint32_t)(w * 32) << 16);
+#pragma unroll 1
+      for (int b4 = 0; b4 < 4; ++b4) {
+        uint4 x[16];
+#pragma unroll
+        for (int e = 0; e < 16; ++e) x[e] = row_ok ? __ldg(ql + 16 * b4 + e) : make_uint4(0, 0, 0, 0);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          uint32_t v[16];
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            v[4 * e] = x[4 * q + e].x; v[4 * e + 1] = x[4 * q + e].y;
+            v[4 * e + 2] = x[4 * q + e].z; v[4 * e + 3] = x[4 * q + e].w;
+          }
+          tmem_st16(lane_addr + 64 * b4 + 16 * q, v);
+        }
+      }
+      const uint4* qr = reinterpret_cast<const uint4*>(a.q_rope + g * a.q_rope_stride);
+      uint4 y[8];
+#pragma unroll
+      for (int c16 = 0; c16 < 8; ++c16) y[c16] = row_ok ? __ldg(qr + c16) : make_uint4(0, 0, 0, 0);
+#pragma unroll
+      for (int c16 = 0; c16 < 8; ++c16)
+        *reinterpret_cast<uint4*>(sm + Q_ROPE + r * 128 + ((c16 ^ (r & 7)) << 4)) = y[c16];
+      tmem_st_wait();
+      fence_async_smem();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&c->q_ready);
+    }
     const uint64_t anc = row_ok ? c->anc[req_row / a.n_heads] : 0ull;
     const float scale2 = a.sm_scale * 1.4426950408889634f;  // scores in log2 units
     float m_ref = -INFINITY, l = 0.f;
@@ -366,14 +451,21 @@ __device__ void scorer(const VerifyArgs& a, const PoolMaps& maps, const Item& it
     const uint32_t peer_pbuf = map_cluster(smem_u32(sm + V_PBUF), acc_rank);
     const uint32_t peer_pfull = map_cluster(smem_u32(&c->pfull[0]), acc_rank);
     const uint32_t lead_sempty = map_cluster(smem_u32(&c->sempty[0]), rank & ~1u);
+    // Index of this lane's key in the next tile (warp w covers keys
+    // 32w .. 32w+31), loaded one tile ahead so the load is off the loop's path.
+    auto tile_has_key = [&](int tile) { return tile < it.ntiles && it.k_begin + tile * TK + 32 * w + lane < it.k_end; };
+    auto tile_key_index = [&](int tile) {
+      return tile_has_key(tile) ? __ldg(a.kv_indices + it.loc.idx_base + it.k_begin + tile * TK + 32 * w + lane) : -1;
+    };
+    int id_next = tile_key_index(0);
     for (int t = 0; t < it.ntiles; ++t) {
       const int s = t & 1;
       const int k0 = it.k_begin + t * TK;
-      {  // valid-key bits of this tile: warp w covers keys 32w .. 32w+31
-        const int kp = k0 + 32 * w + lane;
+      {  // valid-key bits of this tile
+        const int id = id_next;
+        id_next = tile_key_index(t + 1);
         bool v = false;
-        if (kp < it.k_end) {
-          const int id = __ldg(a.kv_indices + it.loc.idx_base + kp);
+        if (tile_has_key(t)) {
           v = id >= 0 && (a.pool_rows <= 0 || id < a.pool_rows);
           if (!v) atomicOr(a.status, DDTREE_ST_BAD_INDEX);
         }
@@ -392,22 +484,28 @@ __device__ void scorer(const VerifyArgs& a, const PoolMaps& maps, const Item& it
       uint32_t km[4];
 #pragma unroll
       for (int q = 0; q < 4; ++q) km[q] = c->key_mask[s][q];
-      const bool plain = (k0 + TK <= it.loc.P) && (k0 + TK <= it.k_end) &&
-                         ((km[0] & km[1] & km[2] & km[3]) == 0xffffffffu);
-      float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-      if (plain && row_ok) {
+      // Visible keys of this row as 4 x 32 bits: a valid index, and for a
+      // tree key (position P + j) node j must be an ancestor of the row's
+      // node (or the node itself).  One select per score applies the mask.
+      uint32_t mw[4];
 #pragma unroll
-        for (int k = 0; k < TK; ++k) mx[k & 3] = fmaxf(mx[k & 3], __uint_as_float(xr[k >> 5][k & 31]));
-      } else {
-#pragma unroll
-        for (int k = 0; k < TK; ++k) {
-          const int kp = k0 + k;
-          bool ok = row_ok && ((km[k >> 5] >> (k & 31)) & 1u);
-          if (ok && kp >= it.loc.P) ok = (anc >> (kp - it.loc.P)) & 1ull;
-          const float v = ok ? __uint_as_float(xr[k >> 5][k & 31]) : -INFINITY;
-          xr[k >> 5][k & 31] = __float_as_uint(v);
-          mx[k & 3] = fmaxf(mx[k & 3], v);
+      for (int q = 0; q < 4; ++q) {
+        uint32_t bits = row_ok ? km[q] : 0u;
+        const int lo = k0 + 32 * q - it.loc.P;  // tree index of key 32q (negative: prefix)
+        if (lo > -32) {
+          uint32_t tree;
+          if (lo >= 0) tree = lo < 64 ? (uint32_t)(anc >> lo) : 0u;
+          else tree = (uint32_t)(anc << (-lo)) | ((1u << (-lo)) - 1u);
+          bits &= tree;
         }
+        mw[q] = bits;
+      }
+      float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+      for (int k = 0; k < TK; ++k) {
+        const float v = ((mw[k >> 5] >> (k & 31)) & 1u) ? __uint_as_float(xr[k >> 5][k & 31]) : -INFINITY;
+        xr[k >> 5][k & 31] = __float_as_uint(v);
+        mx[k & 3] = fmaxf(mx[k & 3], v);
       }
       const float mt = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])) * scale2;
       float alpha = 1.f;
@@ -484,16 +582,19 @@ __device__ void accumulator(const VerifyArgs& a, const PoolMaps& maps, const Ite
       const TileIdx ti = finish_tile_indices(a, raw_next, lane);
       if (t + 1 < it.ntiles) raw_next = raw_tile_indices(a, it, t + 1, lane);
       const MyKeys mk = my_keys(ti, lane, prank, kAccProducers, 0, 32);
-      for (int q = 0; q < 4; ++q, ++n) {
-        const int slot = n % VRING;
+      for (int u = 0; u < 4 / VU; ++u, ++n) {
+        const int slot = n % VUNITS;
         bool ok = true;
-        if (lane == 0) ok = wait_clu(&c->vempty[slot], ((n / VRING) & 1) ^ 1, c, a.status);
+        if (lane == 0) ok = wait_clu(&c->vempty[slot], ((n / VUNITS) & 1) ^ 1, c, a.status);
         if (!__shfl_sync(0xffffffffu, ok, 0)) {
           asm volatile("cp.async.wait_all;" ::: "memory");
           return;
         }
-        fill_chunk(maps, a.kv_pool, sm + V_RING + slot * VCHUNK, 2 * q + par, 0, TK, ti, mk, prank, kAccProducers,
-                   lane, &c->vfull[slot]);
+#pragma unroll 1
+        for (int cc = 0; cc < VU; ++cc)
+          fill_chunk(maps, a.kv_pool, sm + V_RING + slot * VUNIT_BYTES + cc * VCHUNK, 2 * (VU * u + cc) + par, 0, TK,
+                     ti, mk, prank, lane, &c->vfull[slot], VU * u + cc >= kAccLsuChunks);
+        cp_async_mbar_arrive(&c->vfull[slot]);
       }
     }
     asm volatile("cp.async.wait_all;" ::: "memory");
@@ -513,21 +614,25 @@ __device__ void accumulator(const VerifyArgs& a, const PoolMaps& maps, const Ite
         }
         tc_fence_after();
         const uint64_t pdesc = desc_sw128(smem_u32(sm + V_PBUF + s * PBUF), 16, 1024);
-        for (int q = 0; q < 4; ++q, ++n) {
-          const int slot = n % VRING;
-          const uint32_t vph = (n / VRING) & 1;
+        for (int u = 0; u < 4 / VU; ++u, ++n) {
+          const int slot = n % VUNITS;
+          const uint32_t vph = (n / VUNITS) & 1;
           if (!wait_clu(&c->vfull[slot], vph, c, a.status) || !wait_clu(&c->vpeer[slot], vph, c, a.status)) {
             ok = false;
             break;
           }
           fence_async_smem();  // cp.async (generic proxy) data -> tensor-core reads
           tc_fence_after();
-          const uint64_t vdesc = desc_sw128(smem_u32(sm + V_RING + slot * VCHUNK), VCHUNK, 1024);
 #pragma unroll
-          for (int ks = 0; ks < 8; ++ks) {
-            const uint64_t ad = pdesc + (uint64_t)(((ks >> 2) * VCHUNK + (ks & 3) * 32) >> 4);
-            const uint64_t bd = vdesc + (uint64_t)((ks * 2048) >> 4);
-            mma2_ss(tmem + 128 * q, ad, bd, idesc, (t > 0 || ks > 0) ? 1u : 0u);
+          for (int cc = 0; cc < VU; ++cc) {
+            const int q = VU * u + cc;
+            const uint64_t vdesc = desc_sw128(smem_u32(sm + V_RING + slot * VUNIT_BYTES + cc * VCHUNK), VCHUNK, 1024);
+#pragma unroll
+            for (int ks = 0; ks < 8; ++ks) {
+              const uint64_t ad = pdesc + (uint64_t)(((ks >> 2) * VCHUNK + (ks & 3) * 32) >> 4);
+              const uint64_t bd = vdesc + (uint64_t)((ks * 2048) >> 4);
+              mma2_ss(tmem + 128 * q, ad, bd, idesc, (t > 0 || ks > 0) ? 1u : 0u);
+            }
           }
           commit2(&c->vempty[slot], kAccPair);
         }
@@ -543,9 +648,9 @@ __device__ void accumulator(const VerifyArgs& a, const PoolMaps& maps, const Ite
         const int s = t & 1;
         if (!wait_clu(&c->pfull[s], (t >> 1) & 1, c, a.status)) return;
         remote_arrive(lead_ppeer + s * 8);
-        for (int q = 0; q < 4; ++q, ++n) {
-          const int slot = n % VRING;
-          if (!wait_clu(&c->vfull[slot], (n / VRING) & 1, c, a.status)) return;
+        for (int u = 0; u < 4 / VU; ++u, ++n) {
+          const int slot = n % VUNITS;
+          if (!wait_clu(&c->vfull[slot], (n / VUNITS) & 1, c, a.status)) return;
           fence_async_smem();
           remote_arrive(lead_vpeer + slot * 8);
         }
@@ -585,6 +690,7 @@ __device__ void accumulator(const VerifyArgs& a, const PoolMaps& maps, const Ite
         tc_fence_after();
         if (__any_sync(0xffffffffu, alpha != 1.f)) {  // warp-collective TMEM access
           uint32_t v[16];
+#pragma unroll 1
           for (int q = 0; q < 32; ++q) {
             tmem_ld16(lane_addr + 16 * q, v);
 #pragma unroll
@@ -603,25 +709,44 @@ __device__ void accumulator(const VerifyArgs& a, const PoolMaps& maps, const Ite
       if (r == 0 && !stop) remote_arrive(sc_pfree + s * 8);
       if (stop) break;
     }
-    // Epilogue: O_s = O / l, written as fp32 rows of the workspace.
+    // Epilogue: O_s = O / l, written as fp32 rows of the workspace.  Each
+    // 32-column slice of the tile goes TMEM -> registers -> a swizzled
+    // shared-memory box (4 rotating 16 KB boxes in the free value ring) ->
+    // one TMA store, which writes whole rows' slices coalesced and clips
+    // the rows past the request.
     const bool done = wait_clu(&c->mma_done, 0, c, a.status);
     tc_fence_after();
     const int req_row = it.row0 + r;
     const bool row_ok = req_row < a.rows_per_req;
     if (__all_sync(0xffffffffu, done)) {
       const float inv = lfin > 0.f ? 1.f / lfin : 0.f;
-      float* po = a.partial_o + ((size_t)it.slot * a.rows_per_req + (row_ok ? req_row : 0)) * kLatent;
-      uint32_t v[16];
-      for (int q = 0; q < 32; ++q) {
-        tmem_ld16(lane_addr + 16 * q, v);
-        if (row_ok) {
+      const bool store = it.row0 < a.rows_per_req;
+      constexpr int kBox = ROWS * 128;  // 16 KB
+      for (int q = 0; q < kLatent / 32; ++q) {
+        uint8_t* box = sm + V_RING + (q & 3) * kBox;
+        if (q >= 4) {
+          // The store issued from this box four slices ago must have read it.
+          if (r == 0) asm volatile("cp.async.bulk.wait_group.read 3;" ::: "memory");
+          named_bar(2, 128);
+        }
+        uint32_t v[32];
+        tmem_ld32(lane_addr + 32 * q, v);
 #pragma unroll
-          for (int e = 0; e < 16; e += 4)
-            *reinterpret_cast<float4*>(po + 16 * q + e) =
-                make_float4(__uint_as_float(v[e]) * inv, __uint_as_float(v[e + 1]) * inv,
-                            __uint_as_float(v[e + 2]) * inv, __uint_as_float(v[e + 3]) * inv);
+        for (int j = 0; j < 8; ++j)
+          *reinterpret_cast<float4*>(box + r * 128 + ((j ^ (r & 7)) << 4)) =
+              make_float4(__uint_as_float(v[4 * j]) * inv, __uint_as_float(v[4 * j + 1]) * inv,
+                          __uint_as_float(v[4 * j + 2]) * inv, __uint_as_float(v[4 * j + 3]) * inv);
+        fence_async_smem();
+        named_bar(2, 128);
+        if (r == 0 && store) {
+          asm volatile(
+              "cp.async.bulk.tensor.3d.global.shared::cta.tile.bulk_group [%0, {%1, %2, %3}], [%4];\n"
+              "cp.async.bulk.commit_group;" ::"l"(&maps.po), "r"(32 * q), "r"(it.row0), "r"(it.slot),
+              "r"(smem_u32(box))
+              : "memory");
         }
       }
+      if (r == 0) asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
     } else if (row_ok) {
       for (int d = 0; d < kLatent; ++d)
         a.partial_o[((size_t)it.slot * a.rows_per_req + req_row) * kLatent + d] = 0.f;
@@ -651,12 +776,12 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(kThreads, 1)
   // still takes part in the cluster barriers and the pair's TMEM allocation.
 
   if (tid == 0) {
-    for (int i = 0; i < QRING; ++i) {
+    for (int i = 0; i < QUNITS; ++i) {
       mbar_init(&c->kfull[i], 32 * kScorerProducers);
       mbar_init(&c->kpeer[i], 1);
       mbar_init(&c->kempty[i], 1);
     }
-    for (int i = 0; i < VRING; ++i) {
+    for (int i = 0; i < VUNITS; ++i) {
       mbar_init(&c->vfull[i], 32 * kAccProducers);
       mbar_init(&c->vpeer[i], 1);
       mbar_init(&c->vempty[i], 1);
@@ -671,6 +796,7 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(kThreads, 1)
       mbar_init(&c->corr_done[i], 8);
     }
     mbar_init(&c->mma_done, 1);
+    mbar_init(&c->q_ready, 4);
     c->abort = 0;
     fence_mbar_init();
   }
@@ -688,36 +814,6 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
 
-  if (rank < 2 && have && warp >= 4 && warp < 8) {
-    // Q rows -> TMEM (warps 4..7, thread = query row = TMEM lane): latent as
-    // packed bf16 pairs; rope -> shared memory.
-    const int r = tid - 128;
-    const int req_row = it.row0 + r;
-    const bool ok = req_row < a.rows_per_req;
-    const size_t g = (size_t)it.loc.b * a.rows_per_req + (ok ? req_row : 0);
-    const uint4* ql = reinterpret_cast<const uint4*>(a.q_latent + g * a.q_lat_stride);
-    const uint32_t lane_addr = c->tmem_base + ((uint32_t)((warp - 4) * 32) << 16);
-    for (int q = 0; q < 16; ++q) {  // 16 x 16 columns = 512 bf16
-      uint32_t v[16];
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        uint4 x = ok ? __ldg(ql + 4 * q + e) : make_uint4(0, 0, 0, 0);
-        v[4 * e] = x.x; v[4 * e + 1] = x.y; v[4 * e + 2] = x.z; v[4 * e + 3] = x.w;
-      }
-      tmem_st16(lane_addr + 16 * q, v);
-    }
-    tmem_st_wait();
-    const uint4* qr = reinterpret_cast<const uint4*>(a.q_rope + g * a.q_rope_stride);
-#pragma unroll
-    for (int c16 = 0; c16 < 8; ++c16) {
-      uint4 x = ok ? __ldg(qr + c16) : make_uint4(0, 0, 0, 0);
-      *reinterpret_cast<uint4*>(sm + Q_ROPE + r * 128 + ((c16 ^ (r & 7)) << 4)) = x;
-    }
-    fence_async_smem();
-  }
-  tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
   cluster_sync();  // all four CTAs' barriers and TMEM ready before any remote traffic
 
   if (have && it.ntiles > 0) {
@@ -774,6 +870,20 @@ cudaError_t make_pool_maps(const VerifyArgs& a, PoolMaps* m) {
     return cudaErrorInvalidValue;
   if (enc(&m->tile, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, base, dims, strides, box_tile, es,
           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+    return cudaErrorInvalidValue;
+  const cuuint32_t box_row[2] = {64, 1};
+  if (enc(&m->row, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, base, dims, strides, box_row, es,
+          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+    return cudaErrorInvalidValue;
+  // Partial O: [total_splits][rows_per_req][512] fp32; rows past the request
+  // fall outside dimension 1, so a store of a partial row tile is clipped.
+  const cuuint64_t odims[3] = {(cuuint64_t)kLatent, (cuuint64_t)a.rows_per_req, (cuuint64_t)a.total_splits};
+  const cuuint64_t ostrides[2] = {(cuuint64_t)kLatent * 4, (cuuint64_t)a.rows_per_req * kLatent * 4};
+  const cuuint32_t obox[3] = {32, (cuuint32_t)ROWS, 1}, oes[3] = {1, 1, 1};
+  if (enc(&m->po, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, a.partial_o, odims, ostrides, obox, oes,
+          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
     return cudaErrorInvalidValue;
   return cudaSuccess;
