@@ -54,7 +54,7 @@ constexpr int VCHUNK = TK * 128;         // accumulator chunk: 128 keys x 64 col
 // unit: a producer warp signals a unit with one cp.async-tracked arrive, which
 // keeps more bytes in flight per arrive than a barrier per chunk.
 constexpr int QU = 3;                    // scorer chunks per unit (24 KB)
-constexpr int QUNITS = 6;                // scorer unit slots (2 tiles)
+constexpr int QUNITS = 7;                // scorer unit slots (2.3 tiles)
 constexpr int QUNIT_BYTES = QU * SCHUNK;
 constexpr int VU = 2;                    // accumulator chunks per unit (32 KB)
 constexpr int VUNITS = 4;                // accumulator unit slots (2 tiles)
@@ -74,7 +74,7 @@ constexpr uint16_t kScorerPair = 0x3, kAccPair = 0xC;
 
 // Shared-memory map (offsets from a 1024-aligned base).
 constexpr int Q_ROPE = 0;                          // scorer: 16 KB
-constexpr int Q_RING = Q_ROPE + VCHUNK;            // scorer: 6 x 24 KB
+constexpr int Q_RING = Q_ROPE + VCHUNK;            // scorer: 7 x 24 KB
 constexpr int Q_STAGE = Q_RING + QUNITS * QUNIT_BYTES;  // scorer: P staging
 constexpr int Q_END = Q_STAGE + PBUF;
 constexpr int V_PBUF = 0;                          // accumulator: 2 x PBUF
