@@ -8,3 +8,6 @@ from .verify_oracle import (  # noqa: F401
     ancestor_sets, ancestor_mask, ancestor_bits, key_mask, verify_request,
     verify_batched, partial_over_keys, merge_partials,
 )
+from .accept_oracle import (  # noqa: F401
+    argmax_rows, greedy_path, accept_request, accept_batched,
+)

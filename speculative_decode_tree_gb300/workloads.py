@@ -229,3 +229,129 @@ def algorithmic_cost(inp: VerifyInputs) -> dict:
     rows = inp.batch * T * H
     byts += rows * ROW_DIM * 2 + rows * (LATENT_DIM * 2 + 4) + 4 * inp.batch * T
     return dict(bytes=byts, flops=flops)
+
+
+# ---------------------------------------------------------------- acceptance
+@dataclass
+class AcceptInputs:
+    """Inputs of the greedy-acceptance step after a verify forward.
+
+    logits        [B, T+1, V] bf16: row 0 is the target's prediction at the
+                  prefix end, row 1+i its prediction after tree node i
+    draft_tokens  [B, T] int32: the drafted token of each tree node
+    tree_parent   [B, T] int32 (-1 = child of the prefix end, else < i)
+    kv_indices    int32: per request P prefix rows then T tree rows
+    kv_indptr     [B+1] int32, prefix_lens [B] int32
+    planted       [B, T+1] int64: the token given the largest logit of each
+                  row by construction (test bookkeeping only)
+    """
+    logits: torch.Tensor
+    draft_tokens: torch.Tensor
+    tree_parent: torch.Tensor
+    kv_indices: torch.Tensor
+    kv_indptr: torch.Tensor
+    prefix_lens: torch.Tensor
+    planted: torch.Tensor
+    pool_rows: int
+    meta: dict
+
+    @property
+    def batch(self) -> int:
+        return int(self.tree_parent.shape[0])
+
+    @property
+    def n_nodes(self) -> int:
+        return int(self.tree_parent.shape[1])
+
+    @property
+    def vocab(self) -> int:
+        return int(self.logits.shape[2])
+
+
+def make_accept_inputs(name: str, *, batch: int, n_nodes: int, vocab: int, prefixes: List[int],
+                       tree: str, pool_rows: int, p_match: float, seed: int,
+                       planted_logit: float = 10.0) -> AcceptInputs:
+    """Draw one acceptance workload (order: indices -> trees -> logits -> drafts).
+
+    Logits are N(0,1) rounded to bf16, except one planted token per row that
+    gets ``planted_logit`` (far above any N(0,1) draw over the vocabulary, so
+    it is the row's unique largest value).  Among the children of each node
+    (and of the prefix end), with probability ``p_match`` one child, chosen
+    uniformly, drafts the parent row's planted token; every other child
+    drafts a distinct other token.  That gives a tree in which the draft
+    agrees with the target along a random root-to-node path, like a drafter
+    whose guesses are right most of the time.
+    """
+    assert len(prefixes) == batch
+    g = torch.Generator().manual_seed(seed)
+    total = sum(P + n_nodes for P in prefixes)
+    if total > pool_rows:
+        raise ValueError("pool too small for the requests")
+    perm = torch.randperm(pool_rows, generator=g)[:total].to(torch.int32)
+    indptr = [0]
+    for P in prefixes:
+        indptr.append(indptr[-1] + P + n_nodes)
+    parents = []
+    for _ in range(batch):
+        if tree == "chain":
+            parents.append(chain_tree(n_nodes))
+        elif tree == "uniform":
+            parents.append(uniform_tree(n_nodes, g))
+        elif tree == "bounded":
+            parents.append(bounded_tree(n_nodes, g))
+        else:
+            raise ValueError(tree)
+    logits = torch.randn(batch, n_nodes + 1, vocab, generator=g)
+    planted = torch.randint(0, vocab, (batch, n_nodes + 1), generator=g)
+    for b in range(batch):
+        for r in range(n_nodes + 1):
+            logits[b, r, int(planted[b, r])] = planted_logit
+    drafts = torch.empty(batch, n_nodes, dtype=torch.int32)
+    for b in range(batch):
+        par = parents[b]
+        for p in [-1] + list(range(n_nodes)):
+            kids = [c for c in range(n_nodes) if par[c] == p]
+            if not kids:
+                continue
+            target = int(planted[b, 0 if p < 0 else 1 + p])
+            match = kids[int(torch.randint(0, len(kids), (1,), generator=g))] \
+                if float(torch.rand(1, generator=g)) < p_match else -1
+            used = {target}
+            for c in kids:
+                if c == match:
+                    drafts[b, c] = target
+                    continue
+                while True:
+                    tok = int(torch.randint(0, vocab, (1,), generator=g))
+                    if tok not in used:
+                        break
+                used.add(tok)
+                drafts[b, c] = tok
+    return AcceptInputs(
+        logits=_bf16(logits),
+        draft_tokens=drafts,
+        tree_parent=torch.tensor(parents, dtype=torch.int32),
+        kv_indices=perm,
+        kv_indptr=torch.tensor(indptr, dtype=torch.int32),
+        prefix_lens=torch.tensor(prefixes, dtype=torch.int32),
+        planted=planted,
+        pool_rows=pool_rows,
+        meta=dict(tree=tree, p_match=p_match, seed=seed, prefixes=list(prefixes)),
+    )
+
+
+# DeepSeek-V3's vocabulary has 129,280 tokens; prefixes as in the verify workloads.
+ACCEPT_WORKLOADS = {
+    "accept_small": dict(batch=2, n_nodes=8, vocab=1000, prefixes=[16, 40], tree="uniform",
+                         pool_rows=4096, p_match=0.8, seed=10),
+    "accept_long": dict(batch=1, n_nodes=32, vocab=129280, prefixes=[65536], tree="bounded",
+                        pool_rows=262144, p_match=0.9, seed=11),
+    "accept_batch": dict(batch=8, n_nodes=32, vocab=129280, prefixes=MIXED_PREFIXES, tree="bounded",
+                         pool_rows=524288, p_match=0.9, seed=12),
+}
+
+
+def accept_workload(name: str, **overrides) -> AcceptInputs:
+    cfg = dict(ACCEPT_WORKLOADS[name])
+    cfg.update(overrides)
+    return make_accept_inputs(name, **cfg)
