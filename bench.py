@@ -49,7 +49,13 @@ def _args():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-contiguous", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
-    return ap.parse_args()
+    ap.add_argument("--step", choices=["verify", "accept"], default="verify",
+                    help="verify: the verify-attention call (the headline); accept: greedy "
+                         "acceptance + KV commit after it")
+    args = ap.parse_args()
+    if args.step == "accept" and args.workload == "long_scattered":
+        args.workload = "accept_long"
+    return args
 
 
 def _dist():
@@ -415,11 +421,139 @@ def run_ours(args, world, rank, local):
     print(json.dumps(line), flush=True)
 
 
+ACCEPT_METRIC = "greedy tree acceptance + KV commit µs/call (argmax over the target logits, walk, commit)"
+
+
+def run_accept(args, world, rank, local):
+    """Greedy acceptance + commit: device time of one call (CUDA graph, L2
+    flushed between steps), its HBM roofline (one pass over the logits), the
+    end-to-end call with host buffers, and the oracle on the host cores."""
+    from speculative_decode_tree_gb300.build import build
+    from speculative_decode_tree_gb300.runner import DeviceAccept
+    from speculative_decode_tree_gb300.workloads import accept_workload
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if rank == 0 or world == 1:
+        build()
+    _barrier(world)
+    peaks = _peaks()
+    inp = accept_workload(args.workload)
+    da = DeviceAccept(inp, device=str(dev))
+    props = torch.cuda.get_device_properties(dev)
+    l2 = getattr(props, "L2_cache_size", 128 << 20) or (128 << 20)
+    flush = torch.empty(2 * l2 // 4 + 1024, dtype=torch.float32, device=dev)
+    stream = torch.cuda.Stream(device=dev)
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        da.run(stream)
+    stream.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream):
+        da.run(stream)
+
+    def one_step():
+        with torch.cuda.stream(stream):
+            flush.zero_()
+            t0.record(stream)
+            graph.replay()
+            t1.record(stream)
+        stream.synchronize()
+        return t0.elapsed_time(t1) * 1e3
+
+    for _ in range(args.warmup):
+        one_step()
+    _barrier(world)
+    calls = []
+    with ClockSampler(local) as clk:
+        wall0 = time.perf_counter()
+        for _ in range(args.steps):
+            calls.append(one_step())
+            clk.sample()
+        torch.cuda.synchronize()
+        _barrier(world)
+        wall = time.perf_counter() - wall0
+    status = da.status(stream)
+    call_us = _max_over_ranks(world, statistics.median(calls))
+    value = call_us / world
+
+    # Algorithmic bytes: the logits once, drafts + parents + the tree rows'
+    # indices read, the five outputs written.
+    B_, T_, V_ = inp.batch, inp.n_nodes, inp.vocab
+    byts = B_ * (T_ + 1) * V_ * 2 + B_ * T_ * 4 * 3 + B_ * 8 + B_ * 4 * 2 + B_ * T_ * 4 * 3
+    hbm = peaks["hbm_gbs"]
+    achieved = byts / (call_us * 1e-6) / 1e9
+
+    e2e = None
+    if not args.no_e2e:
+        host_in = [t.pin_memory() for t in (inp.logits, inp.draft_tokens, inp.tree_parent)]
+        dev_in = [da.logits, da.draft, da.parent]
+        outs = [da.accept_len, da.next_token, da.accepted_nodes, da.commit_indices, da.freed_indices]
+        host_out = [torch.empty_like(o, device="cpu").pin_memory() for o in outs]
+        h2d = sum(t.numel() * t.element_size() for t in host_in)
+        d2h = sum(t.numel() * t.element_size() for t in host_out)
+        es = []
+        for i in range(args.warmup + args.steps):
+            with torch.cuda.stream(stream):
+                flush.zero_()
+                t0.record(stream)
+                for h, d in zip(host_in, dev_in):
+                    d.copy_(h, non_blocking=True)
+                da.run(stream)
+                for h, d in zip(host_out, outs):
+                    h.copy_(d, non_blocking=True)
+                t1.record(stream)
+            stream.synchronize()
+            if i >= args.warmup:
+                es.append(t0.elapsed_time(t1) * 1e3)
+        e2e = {"value": _max_over_ranks(world, statistics.median(es)) / world, "unit": UNIT,
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        from oracle import accept_batched
+        ts = []
+        tstart = time.perf_counter()
+        while not ts or time.perf_counter() - tstart < min(args.cpu_seconds, 10.0):
+            a = time.perf_counter()
+            accept_batched(inp.logits, inp.draft_tokens, inp.tree_parent, inp.kv_indices, inp.kv_indptr,
+                           inp.prefix_lens)
+            ts.append(time.perf_counter() - a)
+        cpu = {"value": statistics.median(ts) * 1e6, "unit": UNIT, "cores": torch.get_num_threads(),
+               "kind": "oracle", "sample": f"{len(ts)} full {args.workload} calls (numpy/torch CPU), median"}
+    if rank != 0:
+        return
+    line = {
+        "metric": ACCEPT_METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": statistics.mean(calls) / 1e3, "higher_is_better": False,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16 logits, int32 indices", "data": "synthetic",
+        "config": {"workload": args.workload, "batch": B_, "nodes": T_, "vocab": V_,
+                   "prefixes": inp.prefix_lens.tolist(), "tree": inp.meta["tree"],
+                   "l2": "flushed between steps (2x L2 write, outside the timed events)",
+                   "timing": "CUDA graph replay on an explicit stream; CUDA events",
+                   "parallelism": "replicas" if world > 1 else "single GPU"},
+        "p10_us": _pct(calls, 0.1), "p90_us": _pct(calls, 0.9),
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
+                     "frac": achieved / hbm, "traffic": None,
+                     "peak_source": peaks["source"] + " HBM copy (MEASURED_PEAKS.json)",
+                     "kernel": "whole call (argmax pass + walk)"},
+        "alg_bytes": byts, "cpu_baseline": cpu, "e2e": e2e, "clocks": clk.summary(),
+        "gpu_launches": 2 * args.steps, "status_word": status, "wall_s_timed_region": wall,
+        "mean_accept_len": float(da.accept_len.float().mean().item()),
+    }
+    print(json.dumps(line), flush=True)
+
+
 def main():
     args = _args()
     world, rank, local = _dist()
     try:
-        if args.impl == "reference":
+        if args.step == "accept":
+            if args.impl == "reference":
+                print(json.dumps({"impl": "reference", "unavailable": "the reference arm times the verify step only"}))
+            else:
+                run_accept(args, world, rank, local)
+        elif args.impl == "reference":
             run_reference(args, world, rank)
         else:
             run_ours(args, world, rank, local)

@@ -38,7 +38,7 @@ EXPORTS = (
     "ddtree_verify_mla_plan", "ddtree_verify_mla_plan_ex", "ddtree_verify_mla_workspace_size",
     "ddtree_verify_mla", "ddtree_verify_mla_batched", "ddtree_build_ancestor_mask",
     "ddtree_verify_mla_check", "ddtree_status_str", "ddtree_verify_mla_batched_timed",
-    "ddtree_verify_mla_noalloc",
+    "ddtree_verify_mla_noalloc", "ddtree_accept_greedy_workspace_size", "ddtree_accept_greedy",
 )
 
 
@@ -91,6 +91,10 @@ def library() -> ctypes.CDLL:
     L.ddtree_verify_mla_check.argtypes = [vp, vp, ctypes.POINTER(ctypes.c_uint32)]
     L.ddtree_status_str.argtypes = [i32]
     L.ddtree_status_str.restype = ctypes.c_char_p
+    L.ddtree_accept_greedy_workspace_size.argtypes = [i32, i32]
+    L.ddtree_accept_greedy_workspace_size.restype = sz
+    L.ddtree_accept_greedy.argtypes = [i32, i32, i32, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]
+    L.ddtree_accept_greedy.restype = i32
     for name in ("ddtree_verify_mla_plan", "ddtree_verify_mla_plan_ex", "ddtree_verify_mla",
                  "ddtree_verify_mla_batched", "ddtree_build_ancestor_mask", "ddtree_verify_mla_check",
                  "ddtree_verify_mla_batched_timed", "ddtree_verify_mla_noalloc"):
@@ -223,3 +227,29 @@ def ddtree_verify_mla_check(workspace, stream=None) -> int:
     if rc not in (DDTREE_OK, DDTREE_EDEVICE_DATA):
         raise DDTreeError(rc, "ddtree_verify_mla_check")
     return int(v.value)
+
+
+def ddtree_accept_greedy_workspace_size(batch: int, n_nodes: int) -> int:
+    return int(library().ddtree_accept_greedy_workspace_size(int(batch), int(n_nodes)))
+
+
+def ddtree_accept_greedy(logits: torch.Tensor, draft_tokens: torch.Tensor, tree_parent: torch.Tensor,
+                         kv_indices: torch.Tensor, kv_indptr: torch.Tensor, prefix_lens: torch.Tensor,
+                         accept_len: torch.Tensor, next_token: torch.Tensor, accepted_nodes: torch.Tensor,
+                         commit_indices: torch.Tensor, freed_indices: torch.Tensor, workspace: torch.Tensor,
+                         stream=None) -> None:
+    """Greedy acceptance + commit (include/ddtree_accept.h).  logits [B, T+1, V]
+    bf16; the int32 outputs are [B] and [B, T]."""
+    B, T1, V = logits.shape
+    T = T1 - 1
+    if not logits.is_contiguous():
+        raise ValueError("logits must be contiguous")
+    i32 = torch.int32
+    _check(library().ddtree_accept_greedy(
+        B, T, V, _dev(logits, torch.bfloat16, "logits"), _dev(draft_tokens, i32, "draft_tokens"),
+        _dev(tree_parent, i32, "tree_parent"), _dev(kv_indices, i32, "kv_indices"),
+        _dev(kv_indptr, i32, "kv_indptr"), _dev(prefix_lens, i32, "prefix_lens"),
+        _dev(accept_len, i32, "accept_len"), _dev(next_token, i32, "next_token"),
+        _dev(accepted_nodes, i32, "accepted_nodes"), _dev(commit_indices, i32, "commit_indices"),
+        _dev(freed_indices, i32, "freed_indices"), _dev(workspace, torch.uint8, "workspace"),
+        workspace.numel(), _stream(stream)), "accept_greedy")

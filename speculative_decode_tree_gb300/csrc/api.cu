@@ -12,16 +12,11 @@
 
 namespace ddtree {
 namespace {
-
 constexpr int kMaxDevices = 64;
 constexpr int64_t kStatusBytes = 256;
-
-struct DevInfo {
-  bool valid;
-  int sms, major, minor;
-};
 DevInfo g_dev[kMaxDevices];
 std::mutex g_dev_mu;
+}  // namespace
 
 // Cached SM count and compute capability of the current device.
 int current_device_info(DevInfo* out) {
@@ -45,6 +40,8 @@ int current_device_info(DevInfo* out) {
   *out = g_dev[d];
   return DDTREE_OK;
 }
+
+namespace {
 
 // Records a timing event; under stream capture it becomes an event-record
 // node of the graph, so replays time the stages too.

@@ -120,7 +120,34 @@ __device__ __forceinline__ uint64_t ancestor_bits(const int32_t* parent, int i, 
 __device__ __forceinline__ float bf16_lo(uint32_t v) { return __uint_as_float(v << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t v) { return __uint_as_float(v & 0xffff0000u); }
 
+// Cached SM count and compute capability of the current device (api.cu).
+struct DevInfo {
+  bool valid;
+  int sms, major, minor;
+};
+int current_device_info(DevInfo* out);
+
+// Everything the acceptance launch needs (see include/ddtree_accept.h).
+struct AcceptArgs {
+  const uint16_t* logits;   // [B, T+1, V] bf16
+  const int32_t* draft;     // [B, T]
+  const int32_t* parent;    // [B, T]
+  const int32_t* kv_indices;
+  const int32_t* kv_indptr;    // [B+1]
+  const int32_t* prefix_lens;  // [B]
+  uint64_t* keys;           // workspace: [B, T+1] argmax keys, zeroed by the launch sequence
+  uint32_t* tickets;        // workspace: [B] CTAs done per request, zeroed likewise
+  int32_t* accept_len;      // [B]
+  int32_t* next_token;      // [B]
+  int32_t* accepted_nodes;  // [B, T]
+  int32_t* commit_indices;  // [B, T]
+  int32_t* freed_indices;   // [B, T]
+  uint32_t* status;         // workspace offset 0
+  int batch, n_nodes, vocab, num_sms;
+};
+
 // ---- launchers (one per .cu file) ----
+cudaError_t launch_accept(const AcceptArgs& a, cudaStream_t stream);
 cudaError_t launch_partial_simt(const VerifyArgs& a, cudaStream_t stream);
 cudaError_t launch_partial_tc(const VerifyArgs& a, cudaStream_t stream);
 cudaError_t launch_partial_tc2(const VerifyArgs& a, cudaStream_t stream);

@@ -63,3 +63,41 @@ class DeviceVerify:
 
     def status(self, stream=None) -> int:
         return B.ddtree_verify_mla_check(self.workspace, stream)
+
+
+class DeviceAccept:
+    """Device copies of an acceptance workload and its output buffers."""
+
+    def __init__(self, inp, device: str = "cuda"):
+        dev = torch.device(device)
+        self.inp = inp
+        self.logits = inp.logits.to(dev).contiguous()
+        self.draft = inp.draft_tokens.to(dev).contiguous()
+        self.parent = inp.tree_parent.to(dev).contiguous()
+        self.kv_indices = inp.kv_indices.to(dev)
+        self.kv_indptr = inp.kv_indptr.to(dev)
+        self.prefix_lens = inp.prefix_lens.to(dev)
+        nb, nt = inp.batch, inp.n_nodes
+        i32 = torch.int32
+        self.accept_len = torch.empty(nb, dtype=i32, device=dev)
+        self.next_token = torch.empty(nb, dtype=i32, device=dev)
+        self.accepted_nodes = torch.empty(nb, nt, dtype=i32, device=dev)
+        self.commit_indices = torch.empty(nb, nt, dtype=i32, device=dev)
+        self.freed_indices = torch.empty(nb, nt, dtype=i32, device=dev)
+        self.workspace = torch.empty(B.ddtree_accept_greedy_workspace_size(nb, nt), dtype=torch.uint8,
+                                     device=dev)
+
+    def run(self, stream=None) -> None:
+        B.ddtree_accept_greedy(self.logits, self.draft, self.parent, self.kv_indices, self.kv_indptr,
+                               self.prefix_lens, self.accept_len, self.next_token, self.accepted_nodes,
+                               self.commit_indices, self.freed_indices, self.workspace, stream)
+
+    def status(self, stream=None) -> int:
+        return B.ddtree_verify_mla_check(self.workspace, stream)
+
+    def outputs(self) -> dict:
+        return {"accept_len": self.accept_len.cpu().numpy(), "next_token": self.next_token.cpu().numpy(),
+                "accepted_nodes": self.accepted_nodes.cpu().numpy(),
+                "commit_indices": self.commit_indices.cpu().numpy(),
+                "freed_indices": self.freed_indices.cpu().numpy()}
+

@@ -321,10 +321,14 @@ def make_accept_inputs(name: str, *, batch: int, n_nodes: int, vocab: int, prefi
                 if c == match:
                     drafts[b, c] = target
                     continue
-                while True:
+                # A fresh token when the vocabulary has one left, else any
+                # token other than the target (siblings may then repeat).
+                for _ in range(64):
                     tok = int(torch.randint(0, vocab, (1,), generator=g))
                     if tok not in used:
                         break
+                else:
+                    tok = (target + 1) % vocab
                 used.add(tok)
                 drafts[b, c] = tok
     return AcceptInputs(

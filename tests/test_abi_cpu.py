@@ -128,3 +128,28 @@ def test_no_device_reports_unsupported(lib):
     arr = (ctypes.c_int32 * 1)(256)
     rc = lib.ddtree_verify_mla_plan(1, 4, 8, ctypes.cast(arr, ctypes.c_void_p), 1024, ctypes.byref(p))
     assert rc == B.DDTREE_EUNSUPPORTED
+
+
+def test_accept_workspace_size(lib):
+    # status block + keys (8 B per scored row) + counters (4 B per request), each rounded to 256
+    assert B.ddtree_accept_greedy_workspace_size(1, 32) == 256 + 512 + 256
+    assert B.ddtree_accept_greedy_workspace_size(8, 64) == 256 + 4352 + 256
+    for bad in [(0, 4), (1, 0), (1, 65), (1025, 4)]:
+        assert B.ddtree_accept_greedy_workspace_size(*bad) == 0
+
+
+@pytest.mark.parametrize("args", [(0, 4, 100), (1, 0, 100), (1, 65, 100), (1, 4, 0), (1, 4, (1 << 26) + 1)])
+def test_accept_rejects_bad_sizes(lib, args):
+    buf = ctypes.create_string_buffer(4096)
+    p = ctypes.cast(ctypes.addressof(buf) + (-ctypes.addressof(buf)) % 256, ctypes.c_void_p)
+    rc = lib.ddtree_accept_greedy(*args, *([p] * 12), 4096 - 256, None)
+    assert rc == B.DDTREE_EINVAL
+
+
+def test_accept_rejects_null_and_small_workspace(lib):
+    buf = ctypes.create_string_buffer(4096)
+    p = ctypes.cast(ctypes.addressof(buf) + (-ctypes.addressof(buf)) % 256, ctypes.c_void_p)
+    ptrs = [p] * 12
+    assert lib.ddtree_accept_greedy(1, 4, 100, None, *ptrs[1:], 1024, None) == B.DDTREE_EINVAL
+    rc = lib.ddtree_accept_greedy(1, 4, 100, *ptrs, 16, None)
+    assert rc == B.DDTREE_EWORKSPACE
