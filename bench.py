@@ -94,6 +94,26 @@ def _peaks():
     return dict(hbm_gbs=6800.0, bf16_tflops=1900.0, bf16_tflops_sustained=1700.0, source="fallback")
 
 
+# DRAM bytes per launch (dram__bytes_read.sum + dram__bytes_write.sum) from one
+# ncu capture of each dominant kernel, tied to the sha1 of the kernel's source
+# when it was taken (profiles/ has the summaries and commands).  Any other
+# version of the source reports null.
+TRAFFIC = {
+    "k_partial_tc2.cu": ("42c0d2e85708b19d060f94111c9a2522b10505af", 77745664 + 2630656),
+    "k_accept.cu": ("016411fbe872d42040beebcfdb04b0f2d27eef9e", 8556032),
+}
+
+
+def _traffic(source: str):
+    import hashlib
+    sha, byts = TRAFFIC.get(source, (None, None))
+    path = os.path.join(ROOT, "speculative_decode_tree_gb300", "csrc", source)
+    if sha is None or not os.path.exists(path):
+        return None
+    with open(path, "rb") as f:
+        return byts if hashlib.sha1(f.read()).hexdigest() == sha else None
+
+
 class ClockSampler:
     """SM clock and clock-event (throttle) reasons sampled while the timed region runs.
 
@@ -407,7 +427,10 @@ def run_ours(args, world, rank, local):
         "roofline_us": roof_us, "roofline_frac_call": roof_us / call_us,
         "partial_kernel_us": partial_us, "combine_kernel_us": statistics.mean(combines),
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": tc_peak, "unit": "TFLOP/s",
-                     "frac": achieved / tc_peak, "traffic": None,
+                     "frac": achieved / tc_peak,
+                     "traffic": _traffic({1: "k_partial_simt.cu", 2: "k_partial_tc.cu",
+                                          3: "k_partial_tc2.cu"}[dv.plan.kernel])
+                     if args.workload == "long_scattered" else None,
                      "peak_source": peaks["source"] + " bf16 burst (MEASURED_PEAKS.json)",
                      "kernel": "split-KV partial (%s)" % {1: "simt", 2: "tcgen05 pair", 3: "tcgen05 cta_group::2 quad"}[dv.plan.kernel]},
         "alg_bytes": byts, "alg_flops": flops,
@@ -534,7 +557,8 @@ def run_accept(args, world, rank, local):
                    "parallelism": "replicas" if world > 1 else "single GPU"},
         "p10_us": _pct(calls, 0.1), "p90_us": _pct(calls, 0.9),
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
-                     "frac": achieved / hbm, "traffic": None,
+                     "frac": achieved / hbm,
+                     "traffic": _traffic("k_accept.cu") if args.workload == "accept_long" else None,
                      "peak_source": peaks["source"] + " HBM copy (MEASURED_PEAKS.json)",
                      "kernel": "whole call (argmax pass + walk)"},
         "alg_bytes": byts, "cpu_baseline": cpu, "e2e": e2e, "clocks": clk.summary(),
