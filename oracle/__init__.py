@@ -11,3 +11,4 @@ from .verify_oracle import (  # noqa: F401
 from .accept_oracle import (  # noqa: F401
     argmax_rows, greedy_path, accept_request, accept_batched,
 )
+from .relocate_oracle import relocate, relocation_errors  # noqa: F401

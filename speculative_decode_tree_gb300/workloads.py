@@ -359,3 +359,66 @@ def accept_workload(name: str, **overrides) -> AcceptInputs:
     cfg = dict(ACCEPT_WORKLOADS[name])
     cfg.update(overrides)
     return make_accept_inputs(name, **cfg)
+
+
+# ---------------------------------------------------------------- relocation
+@dataclass
+class RelocateInputs:
+    """A churned pool and where each request's rows should move.
+
+    kv_pool    [pool_rows, 576] bf16
+    kv_indices int32: per request its P + T rows, scattered over the lower
+               part of the pool (sampled without replacement)
+    kv_indptr  [B+1] int32
+    dest_base  [B] int32: consecutive free regions in the top part of the pool
+    """
+    kv_pool: torch.Tensor
+    kv_indices: torch.Tensor
+    kv_indptr: torch.Tensor
+    dest_base: torch.Tensor
+    meta: dict
+
+    @property
+    def batch(self) -> int:
+        return int(self.dest_base.shape[0])
+
+    @property
+    def pool_rows(self) -> int:
+        return int(self.kv_pool.shape[0])
+
+
+def make_relocate_inputs(name: str, *, prefixes: List[int], n_nodes: int, pool_rows: int,
+                         seed: int) -> RelocateInputs:
+    """Draw order: pool -> source rows -> (destinations follow from the sizes).
+
+    The top sum(P + T) rows of the pool are the free destination area, one
+    region per request in request order; the sources are sampled without
+    replacement from the rows below it, so no destination holds a source."""
+    g = torch.Generator().manual_seed(seed)
+    sizes = [P + n_nodes for P in prefixes]
+    total = sum(sizes)
+    if 2 * total > pool_rows:
+        raise ValueError("pool too small")
+    pool = _bf16(torch.randn(pool_rows, ROW_DIM, generator=g))
+    src = torch.randperm(pool_rows - total, generator=g)[:total].to(torch.int32)
+    indptr = [0]
+    dest = []
+    for n in sizes:
+        dest.append(pool_rows - total + indptr[-1])
+        indptr.append(indptr[-1] + n)
+    return RelocateInputs(kv_pool=pool, kv_indices=src, kv_indptr=torch.tensor(indptr, dtype=torch.int32),
+                          dest_base=torch.tensor(dest, dtype=torch.int32),
+                          meta=dict(prefixes=list(prefixes), n_nodes=n_nodes, seed=seed))
+
+
+RELOCATE_WORKLOADS = {
+    "relocate_small": dict(prefixes=[0, 17, 300], n_nodes=4, pool_rows=2048, seed=20),
+    "relocate_long": dict(prefixes=[65536], n_nodes=32, pool_rows=262144, seed=21),
+    "relocate_batch": dict(prefixes=MIXED_PREFIXES, n_nodes=32, pool_rows=1048576, seed=22),
+}
+
+
+def relocate_workload(name: str, **overrides) -> RelocateInputs:
+    cfg = dict(RELOCATE_WORKLOADS[name])
+    cfg.update(overrides)
+    return make_relocate_inputs(name, **cfg)
