@@ -49,12 +49,12 @@ def _args():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-contiguous", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
-    ap.add_argument("--step", choices=["verify", "accept"], default="verify",
+    ap.add_argument("--step", choices=["verify", "accept", "relocate"], default="verify",
                     help="verify: the verify-attention call (the headline); accept: greedy "
-                         "acceptance + KV commit after it")
+                         "acceptance + KV commit after it; relocate: Tier-1 KV relocation")
     args = ap.parse_args()
-    if args.step == "accept" and args.workload == "long_scattered":
-        args.workload = "accept_long"
+    if args.workload == "long_scattered" and args.step != "verify":
+        args.workload = {"accept": "accept_long", "relocate": "relocate_long"}[args.step]
     return args
 
 
@@ -568,15 +568,141 @@ def run_accept(args, world, rank, local):
     print(json.dumps(line), flush=True)
 
 
+RELOCATE_METRIC = "Tier-1 KV relocation µs/call (scattered rows -> one contiguous region, indices rewritten)"
+
+
+def run_relocate(args, world, rank, local):
+    """Tier-1 relocation of one request's rows: device time of one call (its
+    indices reset outside the timed events before every step), HBM roofline
+    (each row read once and written once), e2e with host buffers, oracle."""
+    from speculative_decode_tree_gb300 import binding as B
+    from speculative_decode_tree_gb300.build import build
+    from speculative_decode_tree_gb300.workloads import relocate_workload
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if rank == 0 or world == 1:
+        build()
+    _barrier(world)
+    peaks = _peaks()
+    inp = relocate_workload(args.workload)
+    pool = inp.kv_pool.to(dev)
+    orig = inp.kv_indices.to(dev)
+    idx = orig.clone()
+    ptr = inp.kv_indptr.to(dev)
+    dst = inp.dest_base.to(dev)
+    old = torch.empty_like(idx)
+    total = int(inp.kv_indptr[-1])
+    ws = torch.empty(B.ddtree_relocate_kv_workspace_size(inp.pool_rows), dtype=torch.uint8, device=dev)
+    props = torch.cuda.get_device_properties(dev)
+    l2 = getattr(props, "L2_cache_size", 128 << 20) or (128 << 20)
+    flush = torch.empty(2 * l2 // 4 + 1024, dtype=torch.float32, device=dev)
+    stream = torch.cuda.Stream(device=dev)
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        B.ddtree_relocate_kv(pool, idx, ptr, dst, total, ws, old, stream)
+    stream.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream):
+        B.ddtree_relocate_kv(pool, idx, ptr, dst, total, ws, old, stream)
+
+    def one_step():
+        with torch.cuda.stream(stream):
+            idx.copy_(orig)
+            flush.zero_()
+            t0.record(stream)
+            graph.replay()
+            t1.record(stream)
+        stream.synchronize()
+        return t0.elapsed_time(t1) * 1e3
+
+    for _ in range(args.warmup):
+        one_step()
+    _barrier(world)
+    calls = []
+    with ClockSampler(local) as clk:
+        wall0 = time.perf_counter()
+        for _ in range(args.steps):
+            calls.append(one_step())
+            clk.sample()
+        torch.cuda.synchronize()
+        _barrier(world)
+        wall = time.perf_counter() - wall0
+    status = B.ddtree_verify_mla_check(ws, stream)
+    call_us = _max_over_ranks(world, statistics.median(calls))
+    value = call_us / world
+    byts = total * (2 * 1152 + 3 * 4) + inp.batch * 12
+    hbm = peaks["hbm_gbs"]
+    achieved = byts / (call_us * 1e-6) / 1e9
+
+    e2e = None
+    if not args.no_e2e:
+        host_in = [inp.kv_indices.pin_memory(), inp.kv_indptr.pin_memory(), inp.dest_base.pin_memory()]
+        dev_in = [idx, ptr, dst]
+        host_out = [torch.empty_like(idx, device="cpu").pin_memory(), torch.empty_like(old, device="cpu").pin_memory()]
+        h2d = sum(t.numel() * t.element_size() for t in host_in)
+        d2h = sum(t.numel() * t.element_size() for t in host_out)
+        es = []
+        for i in range(args.warmup + args.steps):
+            with torch.cuda.stream(stream):
+                flush.zero_()
+                t0.record(stream)
+                for h, d in zip(host_in, dev_in):
+                    d.copy_(h, non_blocking=True)
+                B.ddtree_relocate_kv(pool, idx, ptr, dst, total, ws, old, stream)
+                host_out[0].copy_(idx, non_blocking=True)
+                host_out[1].copy_(old, non_blocking=True)
+                t1.record(stream)
+            stream.synchronize()
+            if i >= args.warmup:
+                es.append(t0.elapsed_time(t1) * 1e3)
+        e2e = {"value": _max_over_ranks(world, statistics.median(es)) / world, "unit": UNIT,
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        from oracle import relocate
+        ts = []
+        tstart = time.perf_counter()
+        while not ts or time.perf_counter() - tstart < min(args.cpu_seconds, 10.0):
+            a = time.perf_counter()
+            relocate(inp.kv_pool, inp.kv_indices, inp.kv_indptr, inp.dest_base)
+            ts.append(time.perf_counter() - a)
+        cpu = {"value": statistics.median(ts) * 1e6, "unit": UNIT, "cores": torch.get_num_threads(),
+               "kind": "oracle", "sample": f"{len(ts)} full {args.workload} calls (torch CPU, row by row), median"}
+    if rank != 0:
+        return
+    line = {
+        "metric": RELOCATE_METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": statistics.mean(calls) / 1e3, "higher_is_better": False,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16 rows (copied bit for bit), int32 indices",
+        "data": "synthetic",
+        "config": {"workload": args.workload, "batch": inp.batch, "rows": total, "pool_rows": inp.pool_rows,
+                   "l2": "flushed between steps (2x L2 write, outside the timed events)",
+                   "timing": "CUDA graph replay on an explicit stream; CUDA events; indices reset before each step",
+                   "parallelism": "replicas" if world > 1 else "single GPU"},
+        "p10_us": _pct(calls, 0.1), "p90_us": _pct(calls, 0.9),
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
+                     "frac": achieved / hbm,
+                     "traffic": _traffic("k_relocate.cu") if args.workload == "relocate_long" else None,
+                     "peak_source": peaks["source"] + " HBM copy (MEASURED_PEAKS.json)",
+                     "kernel": "whole call (mark + check + copy)"},
+        "alg_bytes": byts, "cpu_baseline": cpu, "e2e": e2e, "clocks": clk.summary(),
+        "gpu_launches": 3 * args.steps, "status_word": status, "wall_s_timed_region": wall,
+    }
+    print(json.dumps(line), flush=True)
+
+
 def main():
     args = _args()
     world, rank, local = _dist()
     try:
-        if args.step == "accept":
-            if args.impl == "reference":
-                print(json.dumps({"impl": "reference", "unavailable": "the reference arm times the verify step only"}))
-            else:
-                run_accept(args, world, rank, local)
+        if args.step != "verify" and args.impl == "reference":
+            print(json.dumps({"impl": "reference", "unavailable": "the reference arm times the verify step only"}))
+        elif args.step == "accept":
+            run_accept(args, world, rank, local)
+        elif args.step == "relocate":
+            run_relocate(args, world, rank, local)
         elif args.impl == "reference":
             run_reference(args, world, rank)
         else:

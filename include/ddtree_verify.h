@@ -77,6 +77,7 @@ enum ddtree_status {
 #define DDTREE_ST_BAD_PARENT  0x2u   /* parent not -1 and not an earlier node */
 #define DDTREE_ST_BAD_LENGTH  0x4u   /* device lengths exceed the plan        */
 #define DDTREE_ST_TIMEOUT     0x8u   /* a bounded wait in a kernel expired    */
+#define DDTREE_ST_OVERLAP     0x10u  /* relocation: a destination row is busy  */
 
 /* Kernel variants of the split-KV partial stage. */
 #define DDTREE_KERNEL_AUTO 0

@@ -28,6 +28,7 @@ DDTREE_ST_BAD_INDEX = 0x1
 DDTREE_ST_BAD_PARENT = 0x2
 DDTREE_ST_BAD_LENGTH = 0x4
 DDTREE_ST_TIMEOUT = 0x8
+DDTREE_ST_OVERLAP = 0x10
 
 DDTREE_KERNEL_AUTO = 0
 DDTREE_KERNEL_SIMT = 1
@@ -39,6 +40,7 @@ EXPORTS = (
     "ddtree_verify_mla", "ddtree_verify_mla_batched", "ddtree_build_ancestor_mask",
     "ddtree_verify_mla_check", "ddtree_status_str", "ddtree_verify_mla_batched_timed",
     "ddtree_verify_mla_noalloc", "ddtree_accept_greedy_workspace_size", "ddtree_accept_greedy",
+    "ddtree_relocate_kv_workspace_size", "ddtree_relocate_kv",
 )
 
 
@@ -95,6 +97,10 @@ def library() -> ctypes.CDLL:
     L.ddtree_accept_greedy_workspace_size.restype = sz
     L.ddtree_accept_greedy.argtypes = [i32, i32, i32, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]
     L.ddtree_accept_greedy.restype = i32
+    L.ddtree_relocate_kv_workspace_size.argtypes = [i64]
+    L.ddtree_relocate_kv_workspace_size.restype = sz
+    L.ddtree_relocate_kv.argtypes = [i32, i64, vp, i64, vp, vp, vp, vp, vp, sz, vp]
+    L.ddtree_relocate_kv.restype = i32
     for name in ("ddtree_verify_mla_plan", "ddtree_verify_mla_plan_ex", "ddtree_verify_mla",
                  "ddtree_verify_mla_batched", "ddtree_build_ancestor_mask", "ddtree_verify_mla_check",
                  "ddtree_verify_mla_batched_timed", "ddtree_verify_mla_noalloc"):
@@ -253,3 +259,20 @@ def ddtree_accept_greedy(logits: torch.Tensor, draft_tokens: torch.Tensor, tree_
         _dev(accepted_nodes, i32, "accepted_nodes"), _dev(commit_indices, i32, "commit_indices"),
         _dev(freed_indices, i32, "freed_indices"), _dev(workspace, torch.uint8, "workspace"),
         workspace.numel(), _stream(stream)), "accept_greedy")
+
+
+def ddtree_relocate_kv_workspace_size(pool_rows: int) -> int:
+    return int(library().ddtree_relocate_kv_workspace_size(int(pool_rows)))
+
+
+def ddtree_relocate_kv(kv_pool: torch.Tensor, kv_indices: torch.Tensor, kv_indptr: torch.Tensor,
+                       dest_base: torch.Tensor, total_rows: int, workspace: torch.Tensor,
+                       old_indices: Optional[torch.Tensor] = None, stream=None) -> None:
+    """Tier-1 relocation (include/ddtree_relocate.h): moves each request's rows
+    to [dest_base[b], dest_base[b] + n_b) and rewrites kv_indices in place."""
+    i32 = torch.int32
+    _check(library().ddtree_relocate_kv(
+        int(dest_base.numel()), int(total_rows), _dev(kv_pool, torch.bfloat16, "kv_pool"), int(kv_pool.shape[0]),
+        _dev(kv_indices, i32, "kv_indices"), _dev(kv_indptr, i32, "kv_indptr"), _dev(dest_base, i32, "dest_base"),
+        None if old_indices is None else _dev(old_indices, i32, "old_indices"),
+        _dev(workspace, torch.uint8, "workspace"), workspace.numel(), _stream(stream)), "relocate_kv")

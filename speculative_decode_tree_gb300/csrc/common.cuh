@@ -1,6 +1,8 @@
 // Shared device-side definitions of the DDTree verify-attention library.
 #pragma once
 
+#include <algorithm>
+
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
@@ -146,7 +148,21 @@ struct AcceptArgs {
   int batch, n_nodes, vocab, num_sms;
 };
 
+// Everything the relocation launches need (see include/ddtree_relocate.h).
+struct RelocateArgs {
+  uint16_t* pool;            // [pool_rows, 576] bf16, updated in place
+  int32_t* indices;          // [total_rows], updated in place
+  const int32_t* indptr;     // [batch+1]
+  const int32_t* dest;       // [batch]
+  int32_t* old_indices;      // [total_rows] or null
+  uint32_t* bitmap;          // workspace: one bit per pool row, zeroed by the launch sequence
+  uint32_t* status;          // workspace offset 0
+  int64_t pool_rows, total_rows;
+  int batch;
+};
+
 // ---- launchers (one per .cu file) ----
+cudaError_t launch_relocate(const RelocateArgs& a, int num_sms, cudaStream_t stream);
 cudaError_t launch_accept(const AcceptArgs& a, cudaStream_t stream);
 cudaError_t launch_partial_simt(const VerifyArgs& a, cudaStream_t stream);
 cudaError_t launch_partial_tc(const VerifyArgs& a, cudaStream_t stream);

@@ -153,3 +153,27 @@ def test_accept_rejects_null_and_small_workspace(lib):
     assert lib.ddtree_accept_greedy(1, 4, 100, None, *ptrs[1:], 1024, None) == B.DDTREE_EINVAL
     rc = lib.ddtree_accept_greedy(1, 4, 100, *ptrs, 16, None)
     assert rc == B.DDTREE_EWORKSPACE
+
+
+def test_relocate_workspace_size(lib):
+    assert B.ddtree_relocate_kv_workspace_size(1) == 256 + 256
+    assert B.ddtree_relocate_kv_workspace_size(262144) == 256 + 32768        # one bit per row
+    assert B.ddtree_relocate_kv_workspace_size(0) == 0
+    assert B.ddtree_relocate_kv_workspace_size(1 << 31) == 0
+
+
+def test_relocate_rejects_bad_arguments(lib):
+    buf = ctypes.create_string_buffer(8192)
+    p = ctypes.cast(ctypes.addressof(buf) + (-ctypes.addressof(buf)) % 256, ctypes.c_void_p)
+    ok = dict(batch=1, total=4, pool=p, rows=100, idx=p, ptr=p, dst=p, old=None, ws=p, wsb=4096)
+
+    def call(**kw):
+        a = dict(ok, **kw)
+        return lib.ddtree_relocate_kv(a["batch"], a["total"], a["pool"], a["rows"], a["idx"], a["ptr"],
+                                      a["dst"], a["old"], a["ws"], a["wsb"], None)
+    assert call(batch=0) == B.DDTREE_EINVAL
+    assert call(rows=0) == B.DDTREE_EINVAL
+    assert call(total=101) == B.DDTREE_EINVAL
+    assert call(pool=None) == B.DDTREE_EINVAL
+    assert call(ptr=ctypes.c_void_p(p.value + 2)) == B.DDTREE_EINVAL
+    assert call(wsb=16) == B.DDTREE_EWORKSPACE
