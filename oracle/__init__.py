@@ -12,3 +12,4 @@ from .accept_oracle import (  # noqa: F401
     argmax_rows, greedy_path, accept_request, accept_batched,
 )
 from .relocate_oracle import relocate, relocation_errors  # noqa: F401
+from .mask_oracle import tree_from_mask, trees_from_flat_mask  # noqa: F401

@@ -422,3 +422,31 @@ def relocate_workload(name: str, **overrides) -> RelocateInputs:
     cfg = dict(RELOCATE_WORKLOADS[name])
     cfg.update(overrides)
     return make_relocate_inputs(name, **cfg)
+
+
+# ---------------------------------------------------------------- tree masks
+def tree_mask(parents: List[int], prefix_len: int) -> torch.Tensor:
+    """The flattened-mask input format for one request: uint8 [T, P + T],
+    row i = 1 for every prefix row and for node i and each node on its parent
+    chain.  (Input construction: the form a serving framework builds on the
+    host and hands over instead of the parent array.)"""
+    T = len(parents)
+    m = torch.zeros(T, prefix_len + T, dtype=torch.uint8)
+    m[:, :prefix_len] = 1
+    for i in range(T):
+        j = i
+        while j >= 0:
+            m[i, prefix_len + j] = 1
+            j = parents[j]
+    return m
+
+
+def flat_tree_masks(tree_parent: torch.Tensor, prefix_lens: torch.Tensor):
+    """All requests' masks concatenated row-major; returns (flat uint8 mask,
+    int64 element offsets [B+1])."""
+    parts, indptr = [], [0]
+    for b in range(tree_parent.shape[0]):
+        m = tree_mask(tree_parent[b].tolist(), int(prefix_lens[b]))
+        parts.append(m.reshape(-1))
+        indptr.append(indptr[-1] + m.numel())
+    return torch.cat(parts), torch.tensor(indptr, dtype=torch.int64)
