@@ -59,7 +59,7 @@ def test_broken_masks_are_caught():
     assert not r["chain_ok"] and r["parents"][3] == 2     # the rule still names the largest seen node
     later = good.copy(); later[1, 2 + 3] = 1              # node 1 sees a later node
     assert not tree_from_mask(later, 2)["chain_ok"]
-    skip = good.copy(); skip[2, 2 + 1] = 0                # node 2 sees node 0 but not its parent 1
+    skip = _nx_mask([-1, 0, 1, 2], 2); skip[3, 2 + 1] = 0  # node 3 sees 2 and 0 but not 1 (2's parent)
     assert not tree_from_mask(skip, 2)["chain_ok"]
     for bad in (no_self, prefix_hole, sibling, later, skip):
         assert not tree_from_mask(bad, 2)["valid"]
