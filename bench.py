@@ -49,12 +49,13 @@ def _args():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-contiguous", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
-    ap.add_argument("--step", choices=["verify", "accept", "relocate"], default="verify",
+    ap.add_argument("--step", choices=["verify", "accept", "relocate", "mask"], default="verify",
                     help="verify: the verify-attention call (the headline); accept: greedy "
-                         "acceptance + KV commit after it; relocate: Tier-1 KV relocation")
+                         "acceptance + KV commit after it; relocate: Tier-1 KV relocation; "
+                         "mask: flattened custom tree mask -> parents")
     args = ap.parse_args()
-    if args.workload == "long_scattered" and args.step != "verify":
-        args.workload = {"accept": "accept_long", "relocate": "relocate_long"}[args.step]
+    if args.workload == "long_scattered" and args.step not in ("verify", "mask"):
+        args.workload = {"accept": "accept_long", "relocate": "relocate_long", "mask": "long_scattered"}[args.step]
     return args
 
 
@@ -693,6 +694,127 @@ def run_relocate(args, world, rank, local):
     print(json.dumps(line), flush=True)
 
 
+MASK_METRIC = "flattened custom tree mask -> parent array µs/call (one pass over the mask)"
+
+
+def run_mask(args, world, rank, local):
+    """Mask reader on the trees and prefixes of a verify workload: device time
+    of one call (graph, L2 flushed), HBM roofline over the mask bytes, e2e
+    with the mask copied from host memory, oracle on the host cores."""
+    from speculative_decode_tree_gb300 import binding as B
+    from speculative_decode_tree_gb300.build import build
+    from speculative_decode_tree_gb300.workloads import flat_tree_masks, workload
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if rank == 0 or world == 1:
+        build()
+    _barrier(world)
+    peaks = _peaks()
+    inp = workload(args.workload)
+    flat_h, indptr_h = flat_tree_masks(inp.tree_parent, inp.prefix_lens)
+    flat, indptr = flat_h.to(dev), indptr_h.to(dev)
+    plen = inp.prefix_lens.to(dev)
+    Bn, T = inp.batch, inp.n_nodes
+    parent = torch.empty(Bn, T, dtype=torch.int32, device=dev)
+    anc = torch.empty(Bn, T, dtype=torch.int64, device=dev)
+    ws = torch.empty(B.ddtree_tree_from_mask_workspace_size(Bn, T), dtype=torch.uint8, device=dev)
+    props = torch.cuda.get_device_properties(dev)
+    l2 = getattr(props, "L2_cache_size", 128 << 20) or (128 << 20)
+    flush = torch.empty(2 * l2 // 4 + 1024, dtype=torch.float32, device=dev)
+    stream = torch.cuda.Stream(device=dev)
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        B.ddtree_tree_from_mask(flat, indptr, plen, parent, ws, anc, stream)
+    stream.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream):
+        B.ddtree_tree_from_mask(flat, indptr, plen, parent, ws, anc, stream)
+
+    def one_step():
+        with torch.cuda.stream(stream):
+            flush.zero_()
+            t0.record(stream)
+            graph.replay()
+            t1.record(stream)
+        stream.synchronize()
+        return t0.elapsed_time(t1) * 1e3
+
+    for _ in range(args.warmup):
+        one_step()
+    _barrier(world)
+    calls = []
+    with ClockSampler(local) as clk:
+        wall0 = time.perf_counter()
+        for _ in range(args.steps):
+            calls.append(one_step())
+            clk.sample()
+        torch.cuda.synchronize()
+        _barrier(world)
+        wall = time.perf_counter() - wall0
+    status = B.ddtree_verify_mla_check(ws, stream)
+    call_us = _max_over_ranks(world, statistics.median(calls))
+    value = call_us / world
+    byts = flat.numel() + (Bn + 1) * 8 + Bn * 4 + Bn * T * (4 + 8)
+    hbm = peaks["hbm_gbs"]
+    achieved = byts / (call_us * 1e-6) / 1e9
+
+    e2e = None
+    if not args.no_e2e:
+        host_in = [flat_h.pin_memory(), indptr_h.pin_memory(), inp.prefix_lens.pin_memory()]
+        dev_in = [flat, indptr, plen]
+        host_out = [torch.empty_like(parent, device="cpu").pin_memory()]
+        h2d = sum(t.numel() * t.element_size() for t in host_in)
+        d2h = sum(t.numel() * t.element_size() for t in host_out)
+        es = []
+        for i in range(args.warmup + args.steps):
+            with torch.cuda.stream(stream):
+                flush.zero_()
+                t0.record(stream)
+                for h, d in zip(host_in, dev_in):
+                    d.copy_(h, non_blocking=True)
+                B.ddtree_tree_from_mask(flat, indptr, plen, parent, ws, anc, stream)
+                host_out[0].copy_(parent, non_blocking=True)
+                t1.record(stream)
+            stream.synchronize()
+            if i >= args.warmup:
+                es.append(t0.elapsed_time(t1) * 1e3)
+        e2e = {"value": _max_over_ranks(world, statistics.median(es)) / world, "unit": UNIT,
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        from oracle import trees_from_flat_mask
+        flat_np, ind_l, pl_l = flat_h.numpy(), indptr_h.tolist(), inp.prefix_lens.tolist()
+        ts = []
+        tstart = time.perf_counter()
+        while not ts or time.perf_counter() - tstart < min(args.cpu_seconds, 10.0):
+            a = time.perf_counter()
+            trees_from_flat_mask(flat_np, ind_l, pl_l, T)
+            ts.append(time.perf_counter() - a)
+        cpu = {"value": statistics.median(ts) * 1e6, "unit": UNIT, "cores": torch.get_num_threads(),
+               "kind": "oracle", "sample": f"{len(ts)} full calls on {args.workload}'s trees (numpy), median"}
+    if rank != 0:
+        return
+    line = {
+        "metric": MASK_METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": statistics.mean(calls) / 1e3, "higher_is_better": False,
+        "scaling": "weak", "vs_baseline": None, "dtype": "u8 mask, int32/u64 outputs", "data": "synthetic",
+        "config": {"workload": args.workload, "batch": Bn, "nodes": T, "prefixes": inp.prefix_lens.tolist(),
+                   "mask_bytes": int(flat.numel()),
+                   "l2": "flushed between steps (2x L2 write, outside the timed events)",
+                   "timing": "CUDA graph replay on an explicit stream; CUDA events",
+                   "parallelism": "replicas" if world > 1 else "single GPU"},
+        "p10_us": _pct(calls, 0.1), "p90_us": _pct(calls, 0.9),
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
+                     "traffic": None, "peak_source": peaks["source"] + " HBM copy (MEASURED_PEAKS.json)",
+                     "kernel": "mask_kernel"},
+        "alg_bytes": byts, "cpu_baseline": cpu, "e2e": e2e, "clocks": clk.summary(),
+        "gpu_launches": args.steps, "status_word": status, "wall_s_timed_region": wall,
+    }
+    print(json.dumps(line), flush=True)
+
+
 def main():
     args = _args()
     world, rank, local = _dist()
@@ -703,6 +825,8 @@ def main():
             run_accept(args, world, rank, local)
         elif args.step == "relocate":
             run_relocate(args, world, rank, local)
+        elif args.step == "mask":
+            run_mask(args, world, rank, local)
         elif args.impl == "reference":
             run_reference(args, world, rank)
         else:

@@ -78,6 +78,7 @@ enum ddtree_status {
 #define DDTREE_ST_BAD_LENGTH  0x4u   /* device lengths exceed the plan        */
 #define DDTREE_ST_TIMEOUT     0x8u   /* a bounded wait in a kernel expired    */
 #define DDTREE_ST_OVERLAP     0x10u  /* relocation: a destination row is busy  */
+#define DDTREE_ST_BAD_MASK    0x20u  /* a custom mask that is not a tree mask  */
 
 /* Kernel variants of the split-KV partial stage. */
 #define DDTREE_KERNEL_AUTO 0

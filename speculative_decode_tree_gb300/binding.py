@@ -29,6 +29,7 @@ DDTREE_ST_BAD_PARENT = 0x2
 DDTREE_ST_BAD_LENGTH = 0x4
 DDTREE_ST_TIMEOUT = 0x8
 DDTREE_ST_OVERLAP = 0x10
+DDTREE_ST_BAD_MASK = 0x20
 
 DDTREE_KERNEL_AUTO = 0
 DDTREE_KERNEL_SIMT = 1
@@ -41,6 +42,7 @@ EXPORTS = (
     "ddtree_verify_mla_check", "ddtree_status_str", "ddtree_verify_mla_batched_timed",
     "ddtree_verify_mla_noalloc", "ddtree_accept_greedy_workspace_size", "ddtree_accept_greedy",
     "ddtree_relocate_kv_workspace_size", "ddtree_relocate_kv",
+    "ddtree_tree_from_mask_workspace_size", "ddtree_tree_from_mask",
 )
 
 
@@ -101,6 +103,10 @@ def library() -> ctypes.CDLL:
     L.ddtree_relocate_kv_workspace_size.restype = sz
     L.ddtree_relocate_kv.argtypes = [i32, i64, vp, i64, vp, vp, vp, vp, vp, sz, vp]
     L.ddtree_relocate_kv.restype = i32
+    L.ddtree_tree_from_mask_workspace_size.argtypes = [i32, i32]
+    L.ddtree_tree_from_mask_workspace_size.restype = sz
+    L.ddtree_tree_from_mask.argtypes = [i32, i32, vp, vp, vp, vp, vp, vp, sz, vp]
+    L.ddtree_tree_from_mask.restype = i32
     for name in ("ddtree_verify_mla_plan", "ddtree_verify_mla_plan_ex", "ddtree_verify_mla",
                  "ddtree_verify_mla_batched", "ddtree_build_ancestor_mask", "ddtree_verify_mla_check",
                  "ddtree_verify_mla_batched_timed", "ddtree_verify_mla_noalloc"):
@@ -276,3 +282,21 @@ def ddtree_relocate_kv(kv_pool: torch.Tensor, kv_indices: torch.Tensor, kv_indpt
         _dev(kv_indices, i32, "kv_indices"), _dev(kv_indptr, i32, "kv_indptr"), _dev(dest_base, i32, "dest_base"),
         None if old_indices is None else _dev(old_indices, i32, "old_indices"),
         _dev(workspace, torch.uint8, "workspace"), workspace.numel(), _stream(stream)), "relocate_kv")
+
+
+def ddtree_tree_from_mask_workspace_size(batch: int, n_nodes: int) -> int:
+    return int(library().ddtree_tree_from_mask_workspace_size(int(batch), int(n_nodes)))
+
+
+def ddtree_tree_from_mask(custom_mask: torch.Tensor, mask_indptr: torch.Tensor, prefix_lens: torch.Tensor,
+                          tree_parent: torch.Tensor, workspace: torch.Tensor,
+                          anc_bits: Optional[torch.Tensor] = None, stream=None) -> None:
+    """Flattened custom tree mask -> parent array (include/ddtree_mask.h).
+    custom_mask uint8 (or bool) flat; tree_parent int32 [B, T] output."""
+    m = custom_mask.view(torch.uint8) if custom_mask.dtype == torch.bool else custom_mask
+    B_, T = tree_parent.shape
+    _check(library().ddtree_tree_from_mask(
+        int(B_), int(T), _dev(m, torch.uint8, "custom_mask"), _dev(mask_indptr, torch.int64, "mask_indptr"),
+        _dev(prefix_lens, torch.int32, "prefix_lens"), _dev(tree_parent, torch.int32, "tree_parent"),
+        None if anc_bits is None else _dev(anc_bits, torch.int64, "anc_bits"),
+        _dev(workspace, torch.uint8, "workspace"), workspace.numel(), _stream(stream)), "tree_from_mask")

@@ -161,7 +161,21 @@ struct RelocateArgs {
   int batch;
 };
 
+// Everything the mask reader needs (see include/ddtree_mask.h).
+struct MaskArgs {
+  const uint8_t* mask;
+  const int64_t* indptr;     // [batch+1] element offsets
+  const int32_t* prefix_lens;
+  int32_t* parent;           // [batch, n_nodes]
+  uint64_t* anc;             // [batch, n_nodes] or null
+  uint64_t* rows;            // workspace: [batch, n_nodes] visible-node bits
+  uint32_t* tickets;         // workspace: [batch]
+  uint32_t* status;          // workspace offset 0
+  int batch, n_nodes, num_sms;
+};
+
 // ---- launchers (one per .cu file) ----
+cudaError_t launch_mask(const MaskArgs& a, cudaStream_t stream);
 cudaError_t launch_relocate(const RelocateArgs& a, int num_sms, cudaStream_t stream);
 cudaError_t launch_accept(const AcceptArgs& a, cudaStream_t stream);
 cudaError_t launch_partial_simt(const VerifyArgs& a, cudaStream_t stream);

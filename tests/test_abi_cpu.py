@@ -177,3 +177,15 @@ def test_relocate_rejects_bad_arguments(lib):
     assert call(pool=None) == B.DDTREE_EINVAL
     assert call(ptr=ctypes.c_void_p(p.value + 2)) == B.DDTREE_EINVAL
     assert call(wsb=16) == B.DDTREE_EWORKSPACE
+
+
+def test_mask_reader_workspace_and_rejections(lib):
+    assert B.ddtree_tree_from_mask_workspace_size(1, 32) == 256 + 256 + 256
+    assert B.ddtree_tree_from_mask_workspace_size(0, 4) == 0
+    assert B.ddtree_tree_from_mask_workspace_size(1, 65) == 0
+    buf = ctypes.create_string_buffer(4096)
+    p = ctypes.cast(ctypes.addressof(buf) + (-ctypes.addressof(buf)) % 256, ctypes.c_void_p)
+    assert lib.ddtree_tree_from_mask(0, 4, p, p, p, p, None, p, 2048, None) == B.DDTREE_EINVAL
+    assert lib.ddtree_tree_from_mask(1, 4, None, p, p, p, None, p, 2048, None) == B.DDTREE_EINVAL
+    assert lib.ddtree_tree_from_mask(1, 4, p, ctypes.c_void_p(p.value + 4), p, p, None, p, 2048, None) == B.DDTREE_EINVAL
+    assert lib.ddtree_tree_from_mask(1, 4, p, p, p, p, None, p, 16, None) == B.DDTREE_EWORKSPACE
