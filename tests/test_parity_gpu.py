@@ -241,3 +241,46 @@ def test_graph_capture_and_replay_with_new_inputs_and_shorter_prefix():
     inp3.kv_indices, inp3.tree_parent = idx_short.to(torch.int32), inp2.tree_parent
     O_ref3, L_ref3 = oracle_rows(inp3, 0)
     assert_within_tolerance(dv.out, dv.lse, O_ref3, L_ref3, "graph replay, shorter prefix")
+
+
+@pytest.mark.parametrize("kernel", KERNELS)
+def test_graph_replay_batched_with_changing_lengths(kernel):
+    """One plan for the longest lengths, captured once; replays with new,
+    shorter and unequal prefix lengths, new indices and new trees must match
+    eager execution bit for bit and the oracle within tolerance."""
+    T, H = 24, 16                                     # 384 rows per request: three row tiles
+    plan_prefixes = [3000, 5000, 800]
+    base = make_inputs("gb", batch=3, n_heads=H, prefixes=plan_prefixes, n_nodes=T, tree="uniform",
+                       pool_rows=32768, index_mode="sample", seed=91)
+    dv = DeviceVerify(base, kernel=kernel)
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        dv.run()
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        dv.run()
+    for step, prefixes in enumerate([[100, 4999, 0], [3000, 1, 800], [2048, 2048, 17]]):
+        new = make_inputs("gb", batch=3, n_heads=H, prefixes=prefixes, n_nodes=T, tree="bounded",
+                          pool_rows=32768, index_mode="sample", seed=92 + step)
+        new.kv_pool = base.kv_pool
+        n = int(new.kv_indptr[-1])
+        dv.q_latent.copy_(new.q_latent)
+        dv.q_rope.copy_(new.q_rope)
+        dv.kv_indices[:n].copy_(new.kv_indices)
+        dv.kv_indptr.copy_(new.kv_indptr)
+        dv.prefix_lens.copy_(new.prefix_lens)
+        dv.tree_parent.copy_(new.tree_parent)
+        g.replay()
+        torch.cuda.synchronize()
+        assert dv.status() == 0, prefixes
+        eager = DeviceVerify(new, kernel=kernel, plan=dv.plan)
+        eager.run()
+        torch.cuda.synchronize()
+        assert torch.equal(eager.out, dv.out) and torch.equal(eager.lse, dv.lse), prefixes
+        for b in range(3):
+            O_ref, L_ref = oracle_rows(new, b)
+            assert_within_tolerance(dv.out[b * T:(b + 1) * T], dv.lse[b * T:(b + 1) * T], O_ref, L_ref,
+                                    f"replay {prefixes} request {b}")
