@@ -119,6 +119,23 @@ __device__ __forceinline__ uint64_t ancestor_bits(const int32_t* parent, int i, 
   return bits;
 }
 
+// The same walk over a parent array already staged in shared memory (one
+// coalesced load instead of a chain of dependent global loads per node).
+__device__ __forceinline__ uint64_t ancestor_bits_smem(const int32_t* parent, int i, int T, uint32_t* status) {
+  uint64_t bits = 0;
+  int a = i;
+  for (int step = 0; step < T && a >= 0; ++step) {
+    bits |= 1ull << a;
+    const int p = parent[a];
+    if (p < -1 || p >= a) {
+      if (status) atomicOr(status, DDTREE_ST_BAD_PARENT);
+      break;
+    }
+    a = p;
+  }
+  return bits;
+}
+
 __device__ __forceinline__ float bf16_lo(uint32_t v) { return __uint_as_float(v << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t v) { return __uint_as_float(v & 0xffff0000u); }
 

@@ -96,9 +96,11 @@ struct __align__(8) Ctrl {
   uint32_t abort;
   uint32_t key_mask[2][4];
   uint64_t anc[64];
+  int32_t par[64];   // the request's parents, staged for the ancestor walk
 };
 
 constexpr size_t kSmemBytes = 1024 + BIG_END + sizeof(Ctrl) + 64;
+static_assert(kSmemBytes <= 227 * 1024, "shared memory per CTA");
 
 __device__ __forceinline__ bool aborted(Ctrl* c) { return *(volatile uint32_t*)&c->abort != 0; }
 __device__ __forceinline__ void set_abort(Ctrl* c, uint32_t* status) {
@@ -806,9 +808,11 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(kThreads, 1)
                  : "memory");
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
   }
+  if (rank < 2 && have && tid < a.n_nodes) c->par[tid] = __ldg(a.tree_parent + (size_t)it.loc.b * a.n_nodes + tid);
+  __syncthreads();
   if (rank < 2 && have) {
     const int T = a.n_nodes;
-    if (tid < T) c->anc[tid] = ancestor_bits(a.tree_parent + (size_t)it.loc.b * T, tid, T, a.status);
+    if (tid < T) c->anc[tid] = ancestor_bits_smem(c->par, tid, T, a.status);
   }
   tc_fence_before();
   __syncthreads();
