@@ -36,19 +36,29 @@ __global__ void mark_kernel(RelocateArgs a) {
     for (int b = 0; b < a.batch && ok; ++b) ok = __ldg(a.indptr + b + 1) >= __ldg(a.indptr + b);
     if (!ok) atomicOr(a.status, DDTREE_ST_BAD_LENGTH);
   }
-  if (g >= a.total_rows) return;
-  const int b = request_of(a.indptr, a.batch, g);
-  const int64_t n = (int64_t)__ldg(a.indptr + b + 1) - __ldg(a.indptr + b);
-  const int64_t k = g - __ldg(a.indptr + b);
-  const int64_t d = __ldg(a.dest + b);
-  if (k < 0 || k >= n) return;  // inconsistent offsets: flagged above
-  if (d < 0 || d + n > a.pool_rows) {
-    atomicOr(a.status, DDTREE_ST_BAD_LENGTH);
-    return;
+  int64_t row = -1;
+  if (g < a.total_rows) {
+    const int b = request_of(a.indptr, a.batch, g);
+    const int64_t n = (int64_t)__ldg(a.indptr + b + 1) - __ldg(a.indptr + b);
+    const int64_t k = g - __ldg(a.indptr + b);
+    const int64_t d = __ldg(a.dest + b);
+    if (k >= 0 && k < n) {  // else: inconsistent offsets, flagged above
+      if (d < 0 || d + n > a.pool_rows) atomicOr(a.status, DDTREE_ST_BAD_LENGTH);
+      else row = d + k;
+    }
   }
-  const int64_t row = d + k;
-  const uint32_t bit = 1u << (row & 31);
-  if (atomicOr(a.bitmap + (row >> 5), bit) & bit) atomicOr(a.status, DDTREE_ST_OVERLAP);
+  // Destination rows are consecutive within a request, so a warp's rows
+  // share one or two bitmap words: one atomic per word, not per row.
+  const uint64_t word = row < 0 ? ~0ull : (uint64_t)(row >> 5);
+  const uint32_t bit = row < 0 ? 0u : 1u << (row & 31);
+  const unsigned peers = __match_any_sync(0xffffffffu, word);
+  const uint32_t bits = __reduce_or_sync(peers, bit);
+  if (row >= 0 && (threadIdx.x & 31) == __ffs(peers) - 1) {
+    // Two lanes with the same row (regions of two requests overlapping
+    // inside this warp) leave fewer bits than lanes.
+    if ((atomicOr(a.bitmap + word, bits) & bits) || __popc(bits) != __popc(peers))
+      atomicOr(a.status, DDTREE_ST_OVERLAP);
+  }
 }
 
 __global__ void check_kernel(RelocateArgs a) {

@@ -127,3 +127,14 @@ def test_two_calls_in_a_row_reuse_the_workspace():
     assert not any(err.values())
     assert torch.equal(idx.cpu(), ref_idx2)
     assert torch.equal(pool.cpu().view(torch.int16), ref_pool2.view(torch.int16))
+
+
+def test_overlapping_destinations_within_one_warp_are_caught():
+    # Two small requests whose destination regions overlap by a few rows that
+    # fall in the same 32-row group (the same warp marks both).
+    inp = relocate_workload("relocate_small", prefixes=[6, 6], n_nodes=2, pool_rows=1024, seed=3)
+    top = int(inp.dest_base[0])
+    bad = _bad(inp, dest_base=torch.tensor([top, top + 5], dtype=torch.int32))
+    pool, idx, old, status = _run(bad)
+    assert status & B.DDTREE_ST_OVERLAP
+    assert torch.equal(idx.cpu(), bad.kv_indices)
