@@ -100,8 +100,9 @@ def _peaks():
 # when it was taken (profiles/ has the summaries and commands).  Any other
 # version of the source reports null.
 TRAFFIC = {
-    "k_partial_tc2.cu": ("42c0d2e85708b19d060f94111c9a2522b10505af", 77745664 + 2630656),
+    "k_partial_tc2.cu": ("3702c8c950cf3dbe3bb95f804271f9fde72ce4d5", 77751808 + 3028480),
     "k_accept.cu": ("016411fbe872d42040beebcfdb04b0f2d27eef9e", 8556032),
+    "k_mask.cu": ("35de2ba635e46a78af91ca088bc100827946414a", 2114000),
 }
 
 
@@ -807,7 +808,8 @@ def run_mask(args, world, rank, local):
                    "parallelism": "replicas" if world > 1 else "single GPU"},
         "p10_us": _pct(calls, 0.1), "p90_us": _pct(calls, 0.9),
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
-                     "traffic": None, "peak_source": peaks["source"] + " HBM copy (MEASURED_PEAKS.json)",
+                     "traffic": _traffic("k_mask.cu") if args.workload == "long_scattered" else None,
+                     "peak_source": peaks["source"] + " HBM copy (MEASURED_PEAKS.json)",
                      "kernel": "mask_kernel"},
         "alg_bytes": byts, "cpu_baseline": cpu, "e2e": e2e, "clocks": clk.summary(),
         "gpu_launches": args.steps, "status_word": status, "wall_s_timed_region": wall,
