@@ -76,10 +76,13 @@ def _barrier(world):
 
 
 def _max_over_ranks(world, x: float) -> float:
+    """The slowest rank's value (the timing rule for replicas); a host-side
+    scalar exchange, on the GPU for NCCL groups and on the CPU for gloo."""
     if world == 1:
         return x
     import torch.distributed as dist
-    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
 
