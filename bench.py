@@ -103,7 +103,7 @@ def _peaks():
 # when it was taken (profiles/ has the summaries and commands).  Any other
 # version of the source reports null.
 TRAFFIC = {
-    "k_partial_tc2.cu": ("3702c8c950cf3dbe3bb95f804271f9fde72ce4d5", 77751808 + 3028480),
+    "k_partial_tc2.cu": ("18e42f977231ddf686e5cd87d003743f4631608a", 77938688 + 2921728),
     "k_accept.cu": ("016411fbe872d42040beebcfdb04b0f2d27eef9e", 8556032),
     "k_mask.cu": ("35de2ba635e46a78af91ca088bc100827946414a", 2114000),
 }

@@ -307,13 +307,8 @@ __device__ void scorer(const VerifyArgs& a, const PoolMaps& maps, const Item& it
           fence_async_smem();  // cp.async (generic proxy) data -> tensor-core reads
           tc_fence_after();
           const uint64_t kdesc = desc_sw128(smem_u32(sm + Q_RING + slot * CHUNK), 16, 1024);
-#pragma unroll
-          for (int kk = 0; kk < 4; ++kk) {
-            const int ks = ch * 4 + kk;
-            const uint64_t bd = kdesc + (uint64_t)((kk * 32) >> 4);
-            if (ch < 8) mma_ts(sbuf, tmem + ks * 8, bd, idesc, ks > 0);
-            else mma_ss(sbuf, rope_desc + (uint64_t)((kk * 32) >> 4), bd, idesc, 1);
-          }
+          if (ch < 8) mma_ts_x4(sbuf, tmem + ch * 32, kdesc, idesc, ch > 0);  // latent: Q from TMEM
+          else mma_ss_x4<2, 2>(sbuf, rope_desc, kdesc, idesc, 1);            // rope: Q from shared memory
           mma_commit(&c->kempty[slot]);
         }
         if (ok) mma_commit(&c->sfull[s]);
@@ -487,12 +482,10 @@ __device__ void accumulator(const VerifyArgs& a, const PoolMaps& maps, const Ite
           fence_async_smem();  // cp.async (generic proxy) data -> tensor-core reads
           tc_fence_after();
           const uint64_t vdesc = desc_sw128(smem_u32(sm + V_RING + slot * 2 * CHUNK), CHUNK, 1024);
-#pragma unroll
-          for (int ks = 0; ks < 8; ++ks) {
-            const uint64_t ad = pdesc + (uint64_t)(((ks >> 2) * CHUNK + (ks & 3) * 32) >> 4);
-            const uint64_t bd = vdesc + (uint64_t)((ks * 2048) >> 4);
-            mma_ss(tmem + 128 * q, ad, bd, idesc, (t > 0 || ks > 0) ? 1u : 0u);
-          }
+          // K steps 0..3 read P atom 0 (keys 0..63), 4..7 atom 1; V advances
+          // 16 keys (2 KB) per step.
+          mma_ss_x4<2, 128>(tmem + 128 * q, pdesc, vdesc, idesc, t > 0 ? 1u : 0u);
+          mma_ss_x4<2, 128>(tmem + 128 * q, pdesc + (CHUNK >> 4), vdesc + 512, idesc, 1u);
           mma_commit(&c->vempty[slot]);
         }
         if (ok) mma_commit(&c->pvdone[s]);

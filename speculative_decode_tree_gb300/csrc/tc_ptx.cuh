@@ -116,20 +116,39 @@ __device__ __forceinline__ uint64_t desc_sw128(uint32_t saddr, uint32_t lbo_byte
   return d;
 }
 
-__device__ __forceinline__ void mma_ss(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
-                                       uint32_t accumulate) {
+// Four K steps (K = 16 each) of one 64-column chunk per statement, the
+// operand addresses stepped inside PTX: one M = 128, N = 128 MMA is 64 tensor
+// cycles, and issuing it with its own statement and C++ descriptor
+// arithmetic costs more than that.  A from TMEM advances 8 columns (16 bf16)
+// per K step, a descriptor ASTEP / BSTEP 16-byte units.
+__device__ __forceinline__ void mma_ts_x4(uint32_t d_tmem, uint32_t a0, uint64_t b0, uint32_t idesc,
+                                          uint32_t acc_first) {
   asm volatile(
-      "{ .reg .pred p; setp.ne.b32 p, %4, 0;\n"
-      "  tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p; }" ::"r"(d_tmem),
-      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      "{ .reg .pred p; .reg .b32 a1, a2, a3; .reg .b64 b1, b2, b3;\n"
+      "  setp.ne.b32 p, %4, 0;\n"
+      "  add.u32 a1, %1, 8; add.u32 a2, %1, 16; add.u32 a3, %1, 24;\n"
+      "  add.u64 b1, %2, 2; add.u64 b2, %2, 4; add.u64 b3, %2, 6;\n"
+      "  tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n"
+      "  tcgen05.mma.cta_group::1.kind::f16 [%0], [a1], b1, %3, 1;\n"
+      "  tcgen05.mma.cta_group::1.kind::f16 [%0], [a2], b2, %3, 1;\n"
+      "  tcgen05.mma.cta_group::1.kind::f16 [%0], [a3], b3, %3, 1; }" ::"r"(d_tmem),
+      "r"(a0), "l"(b0), "r"(idesc), "r"(acc_first)
       : "memory");
 }
-__device__ __forceinline__ void mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
-                                       uint32_t accumulate) {
+template <int ASTEP, int BSTEP>
+__device__ __forceinline__ void mma_ss_x4(uint32_t d_tmem, uint64_t a0, uint64_t b0, uint32_t idesc,
+                                          uint32_t acc_first) {
   asm volatile(
-      "{ .reg .pred p; setp.ne.b32 p, %4, 0;\n"
-      "  tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p; }" ::"r"(d_tmem),
-      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      "{ .reg .pred p; .reg .b64 a1, a2, a3, b1, b2, b3;\n"
+      "  setp.ne.b32 p, %4, 0;\n"
+      "  add.u64 a1, %1, %5; add.u64 a2, %1, %6; add.u64 a3, %1, %7;\n"
+      "  add.u64 b1, %2, %8; add.u64 b2, %2, %9; add.u64 b3, %2, %10;\n"
+      "  tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n"
+      "  tcgen05.mma.cta_group::1.kind::f16 [%0], a1, b1, %3, 1;\n"
+      "  tcgen05.mma.cta_group::1.kind::f16 [%0], a2, b2, %3, 1;\n"
+      "  tcgen05.mma.cta_group::1.kind::f16 [%0], a3, b3, %3, 1; }" ::"r"(d_tmem),
+      "l"(a0), "l"(b0), "r"(idesc), "r"(acc_first), "n"(ASTEP), "n"(2 * ASTEP), "n"(3 * ASTEP), "n"(BSTEP),
+      "n"(2 * BSTEP), "n"(3 * BSTEP)
       : "memory");
 }
 // Arrive once on `bar` when every MMA this thread issued before has completed.
