@@ -106,6 +106,8 @@ TRAFFIC = {
     "k_partial_tc2.cu": ("18e42f977231ddf686e5cd87d003743f4631608a", 77938688 + 2921728),
     "k_accept.cu": ("016411fbe872d42040beebcfdb04b0f2d27eef9e", 8556032),
     "k_mask.cu": ("35de2ba635e46a78af91ca088bc100827946414a", 2114000),
+    # mark + check + copy of one relocate_long call
+    "k_relocate.cu": ("da69118f77628fdfc09c46764f90ab939e28b300", 13677 + 290407 + 75807700 + 13497894),
 }
 
 
