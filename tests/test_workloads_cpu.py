@@ -107,3 +107,20 @@ def test_bounded_tree_respects_both_limits_at_full_size():
         for p in parent:
             kids[p] = kids.get(p, 0) + 1
         assert max(kids.values()) <= 4 and max(_depths(parent)) <= 8
+
+
+# Algorithmic bytes and GFLOP per call from the scope table of the verify path
+# (bytes = sum (P+T)(1152+4) + T H (1152 + 1028) + 4T, FLOPs = H (T P + sum depth) 2176,
+# worked out there for one sample tree per config): the roofline denominators
+# the benchmark divides by must agree with them.
+TABLE = {"tiny": (0.37, 0.018), "tp8_slice": (5.03, 1.14), "long_scattered": (76.4, 36.5),
+         "unsharded_heads": (55.8, 584.0), "mixed_batch": (523.0, 250.0)}
+
+
+@pytest.mark.parametrize("name", sorted(TABLE))
+def test_algorithmic_cost_matches_the_scope_table(name):
+    from speculative_decode_tree_gb300.workloads import algorithmic_cost
+    mb, gflop = TABLE[name]
+    c = algorithmic_cost(workload(name))
+    assert abs(c["bytes"] / 1e6 - mb) <= 0.01 * mb, c
+    assert abs(c["flops"] / 1e9 - gflop) <= 0.01 * gflop, c
