@@ -23,8 +23,10 @@
  *    are DEVICE pointers; *_host pointers are host pointers.
  *  - bf16 tensors are passed as raw 16-bit patterns (ddtree_bf16_t).
  *  - Ownership: the caller owns every buffer, including the workspace.  The
- *    library allocates nothing and keeps no global state beyond a per-device
- *    cache of the SM count and compute capability.  All device work is
+ *    library allocates nothing at run time and keeps no global state beyond
+ *    a per-device cache of the SM count and compute capability; its device
+ *    image holds one fixed scratch array (DDTREE_NOALLOC_SCRATCH_BYTES, used
+ *    only by ddtree_verify_mla_noalloc) on every GPU that loads it.  All device work is
  *    enqueued on the caller's `stream`; there is no host synchronisation
  *    (except in ddtree_verify_mla_check, by design), so calls can be
  *    captured into a CUDA graph.  `out` and `lse` are fully overwritten.
@@ -93,8 +95,9 @@ enum ddtree_status {
  * GPU starved): each request's key sequence (P_b prefix keys, then T tree
  * keys) is cut into chunks of `chunk_keys`; one chunk of one row tile is one
  * work item; `chunk_keys` is chosen so that work items fill the SMs.
- * Fields are outputs of ddtree_verify_mla_plan except the two q strides,
- * which the caller may set afterwards (0 = contiguous rows).
+ * Fields are outputs of ddtree_verify_mla_plan except the two q strides and
+ * wait_limit_us, which the caller may set afterwards (0 = contiguous rows,
+ * 0 = the default 2 s bound).
  */
 typedef struct ddtree_plan {
   int32_t batch;            /* B                                              */
@@ -113,9 +116,18 @@ typedef struct ddtree_plan {
   int32_t q_latent_row_stride; /* elements between (t,h) rows; 0 -> 512       */
   int32_t q_rope_row_stride;   /* elements between (t,h) rows; 0 -> 64        */
   int64_t workspace_bytes;  /* bytes the workspace must hold                  */
-  int64_t off_partial_lse;  /* byte offsets inside the workspace              */
-  int64_t off_partial_o;
-  int32_t reserved[8];
+  int64_t off_partial_lse;  /* byte offsets inside the workspace: fp32 LSEs   */
+  int64_t off_partial_o;    /*   [splits, rows], bf16 partial O [splits, rows, 512] */
+  int32_t fused_combine;    /* 1: the partial kernel merges the splits itself
+                               (cluster-of-four kernel, every cluster resident
+                               at once: a cooperative launch); 0: a separate
+                               combine kernel follows                       */
+  int32_t wait_limit_us;    /* bound of each wait inside the cluster-of-four
+                               kernel, in microseconds; 0 = 2 s.  A wait that
+                               expires sets DDTREE_ST_TIMEOUT and the call
+                               finishes with zero outputs (caller-settable,
+                               e.g. to test that path)                      */
+  int32_t reserved[6];
 } ddtree_plan_t;
 
 /*
@@ -238,25 +250,29 @@ DDTREE_API int ddtree_verify_mla_check(const void* workspace, struct CUstream_st
  *
  * Arguments, layouts and results are those of ddtree_verify_mla without the
  * workspace.  The split-KV partials go to a scratch array built into the
- * library: DDTREE_NOALLOC_SCRATCH_BYTES (32 MiB) of device memory that every
+ * library: DDTREE_NOALLOC_SCRATCH_BYTES (8 MiB) of device memory that every
  * GPU loading the library keeps until the process exits.  When the usual
  * plan would need more scratch than that, the call uses fewer, longer KV
- * splits; a shape that does not fit even with one split per request returns
- * DDTREE_EWORKSPACE (with the current limits of 64 nodes x 128 heads every
- * accepted shape fits).
+ * splits; a shape whose partials do not fit even with one split (more than
+ * about 8,100 query rows, e.g. 64 nodes x 128 heads) returns
+ * DDTREE_EWORKSPACE without launching anything.
  *  - The first call on each device looks up the scratch array's device
  *    address (cudaGetSymbolAddress, which can load the module); make that
  *    first call before any stream capture.
  *  - All calls on a device share the one scratch array, which keeps the
- *    previous call's contents; each call clears the status word it uses and
+ *    previous call's contents; each call clears the status words it uses and
  *    writes every partial it reads.  Calls whose GPU work overlaps (other
  *    streams, other host threads) race on the array: serialise them.
- *  - The status word lives in the library's scratch, so device-data errors
- *    are not observable through this entry point; indices are not checked
- *    against the pool size (as in ddtree_verify_mla).
+ *  - The status word lives in the library's scratch, so neither device-data
+ *    errors nor expired waits (DDTREE_ST_TIMEOUT) are observable through
+ *    this entry point; indices are not checked against the pool size (as in
+ *    ddtree_verify_mla).
+ *  - The cached scratch address belongs to the device's context of the
+ *    first call: do not use this entry point across a device reset
+ *    (cudaDeviceReset) in the same process.
  *  - Calls no cudaMalloc, cudaFree or allocating library routine.
  */
-#define DDTREE_NOALLOC_SCRATCH_BYTES (32u << 20)
+#define DDTREE_NOALLOC_SCRATCH_BYTES (8u << 20)
 DDTREE_API int ddtree_verify_mla_noalloc(const ddtree_bf16_t* q_latent, const ddtree_bf16_t* q_rope,
                               const ddtree_bf16_t* kv_pool, const int32_t* kv_indices,
                               int prefix_len, const int32_t* tree_parent,

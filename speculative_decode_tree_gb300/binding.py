@@ -55,7 +55,8 @@ class Plan(ctypes.Structure):
         ("row_tile", ctypes.c_int32), ("row_tiles", ctypes.c_int32), ("num_sms", ctypes.c_int32),
         ("q_latent_row_stride", ctypes.c_int32), ("q_rope_row_stride", ctypes.c_int32),
         ("workspace_bytes", ctypes.c_int64), ("off_partial_lse", ctypes.c_int64),
-        ("off_partial_o", ctypes.c_int64), ("reserved", ctypes.c_int32 * 8),
+        ("off_partial_o", ctypes.c_int64), ("fused_combine", ctypes.c_int32),
+        ("wait_limit_us", ctypes.c_int32), ("reserved", ctypes.c_int32 * 6),
     ]
 
     def as_dict(self) -> dict:
@@ -119,11 +120,39 @@ def _ptr(t: Optional[torch.Tensor]) -> Optional[int]:
     return None if t is None else t.data_ptr()
 
 
-def _dev(t: torch.Tensor, dtype: torch.dtype, name: str) -> int:
+def _dev(t: torch.Tensor, dtype: torch.dtype, name: str, numel: Optional[int] = None,
+         contiguous: bool = True) -> int:
+    """Device pointer of `t` after checking what the kernels rely on: a CUDA
+    tensor of `dtype` on the current device, contiguous (unless the caller
+    checks its layout), holding at least `numel` elements.  The C ABI trusts
+    the sizes it derives itself, so an undersized or foreign buffer is
+    rejected here, before any launch."""
     if not isinstance(t, torch.Tensor) or not t.is_cuda:
         raise TypeError(f"{name} must be a CUDA tensor")
     if t.dtype != dtype:
         raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if t.device.index != torch.cuda.current_device():
+        raise ValueError(f"{name} is on {t.device}, not the current device cuda:{torch.cuda.current_device()}")
+    if contiguous and not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if numel is not None and t.numel() < numel:
+        raise ValueError(f"{name} holds {t.numel()} elements, needs at least {numel}")
+    return t.data_ptr()
+
+
+def _q(t: torch.Tensor, name: str, rows: int, width: int, row_stride: int) -> int:
+    """Pointer of a query operand: `rows` rows of `width` bf16 values whose
+    starts are `row_stride` elements apart (width when 0), e.g. views
+    q[..., :512] and q[..., 512:] of one [tokens, heads, 576] tensor."""
+    stride = row_stride or width
+    _dev(t, torch.bfloat16, name, contiguous=False)
+    if t.dim() < 2 or t.shape[-1] != width or t.stride(-1) != 1 or t.numel() != rows * width:
+        raise ValueError(f"{name} must be [..., {width}] with {rows} rows of unit-stride elements")
+    expect = stride
+    for d in range(t.dim() - 2, -1, -1):  # every leading dimension steps whole rows
+        if t.shape[d] > 1 and t.stride(d) != expect:
+            raise ValueError(f"{name}: row stride must be {stride} elements (plan q_*_row_stride)")
+        expect *= t.shape[d]
     return t.data_ptr()
 
 
@@ -169,11 +198,17 @@ def ddtree_verify_mla(q_latent, q_rope, kv_pool, kv_indices, prefix_len: int, tr
                       n_nodes: int, n_heads: int, sm_scale: float, out, lse, workspace,
                       stream=None) -> None:
     bf, i32 = torch.bfloat16, torch.int32
-    rc = library().ddtree_verify_mla(
-        _dev(q_latent, bf, "q_latent"), _dev(q_rope, bf, "q_rope"), _dev(kv_pool, bf, "kv_pool"),
-        _dev(kv_indices, i32, "kv_indices"), int(prefix_len), _dev(tree_parent, i32, "tree_parent"),
-        int(n_nodes), int(n_heads), float(sm_scale), _dev(out, bf, "out"),
-        _dev(lse, torch.float32, "lse"), _dev(workspace, torch.uint8, "workspace"), _stream(stream))
+    lib = library()
+    rows = int(n_nodes) * int(n_heads)
+    args = (_dev(q_latent, bf, "q_latent", rows * 512), _dev(q_rope, bf, "q_rope", rows * 64),
+            _dev(kv_pool, bf, "kv_pool"), _dev(kv_indices, i32, "kv_indices", int(prefix_len) + int(n_nodes)),
+            int(prefix_len), _dev(tree_parent, i32, "tree_parent", int(n_nodes)),
+            int(n_nodes), int(n_heads), float(sm_scale), _dev(out, bf, "out", rows * 512),
+            _dev(lse, torch.float32, "lse", rows))
+    # The workspace must hold what the library's own plan for this shape needs.
+    plan = ddtree_verify_mla_plan(1, n_nodes, n_heads, [prefix_len], 0)
+    rc = lib.ddtree_verify_mla(*args, _dev(workspace, torch.uint8, "workspace", plan.workspace_bytes),
+                               _stream(stream))
     _check(rc, "ddtree_verify_mla")
 
 
@@ -183,25 +218,35 @@ def ddtree_verify_mla_noalloc(q_latent, q_rope, kv_pool, kv_indices, prefix_len:
     """ddtree_verify_mla without a workspace: for callers that cannot allocate
     device memory; the partials use the library's built-in scratch array."""
     bf, i32 = torch.bfloat16, torch.int32
+    rows = int(n_nodes) * int(n_heads)
     rc = library().ddtree_verify_mla_noalloc(
-        _dev(q_latent, bf, "q_latent"), _dev(q_rope, bf, "q_rope"), _dev(kv_pool, bf, "kv_pool"),
-        _dev(kv_indices, i32, "kv_indices"), int(prefix_len), _dev(tree_parent, i32, "tree_parent"),
-        int(n_nodes), int(n_heads), float(sm_scale), _dev(out, bf, "out"),
-        _dev(lse, torch.float32, "lse"), _stream(stream))
+        _dev(q_latent, bf, "q_latent", rows * 512), _dev(q_rope, bf, "q_rope", rows * 64),
+        _dev(kv_pool, bf, "kv_pool"), _dev(kv_indices, i32, "kv_indices", int(prefix_len) + int(n_nodes)),
+        int(prefix_len), _dev(tree_parent, i32, "tree_parent", int(n_nodes)),
+        int(n_nodes), int(n_heads), float(sm_scale), _dev(out, bf, "out", rows * 512),
+        _dev(lse, torch.float32, "lse", rows), _stream(stream))
     _check(rc, "ddtree_verify_mla_noalloc")
+
+
+def _batched_args(plan: Plan, q_latent, q_rope, kv_pool, kv_indices, kv_indptr, prefix_lens, tree_parent,
+                  sm_scale, out, lse, workspace):
+    bf, i32 = torch.bfloat16, torch.int32
+    b, t, rows = plan.batch, plan.n_nodes, plan.batch * plan.rows_per_req
+    pool_numel = plan.pool_rows * 576 if plan.pool_rows > 0 else None
+    return (ctypes.byref(plan), _q(q_latent, "q_latent", rows, 512, plan.q_latent_row_stride),
+            _q(q_rope, "q_rope", rows, 64, plan.q_rope_row_stride), _dev(kv_pool, bf, "kv_pool", pool_numel),
+            _dev(kv_indices, i32, "kv_indices"), _dev(kv_indptr, i32, "kv_indptr", b + 1),
+            _dev(prefix_lens, i32, "prefix_lens", b), _dev(tree_parent, i32, "tree_parent", b * t),
+            float(sm_scale), _dev(out, bf, "out", rows * 512), _dev(lse, torch.float32, "lse", rows),
+            _dev(workspace, torch.uint8, "workspace", plan.workspace_bytes), workspace.numel())
 
 
 def ddtree_verify_mla_batched(plan: Plan, q_latent, q_rope, kv_pool, kv_indices, kv_indptr,
                               prefix_lens, tree_parent, sm_scale: float, out, lse, workspace,
                               stream=None) -> None:
-    bf, i32 = torch.bfloat16, torch.int32
     rc = library().ddtree_verify_mla_batched(
-        ctypes.byref(plan), _dev(q_latent, bf, "q_latent"), _dev(q_rope, bf, "q_rope"),
-        _dev(kv_pool, bf, "kv_pool"), _dev(kv_indices, i32, "kv_indices"),
-        _dev(kv_indptr, i32, "kv_indptr"), _dev(prefix_lens, i32, "prefix_lens"),
-        _dev(tree_parent, i32, "tree_parent"), float(sm_scale), _dev(out, bf, "out"),
-        _dev(lse, torch.float32, "lse"), _dev(workspace, torch.uint8, "workspace"),
-        workspace.numel(), _stream(stream))
+        *_batched_args(plan, q_latent, q_rope, kv_pool, kv_indices, kv_indptr, prefix_lens, tree_parent,
+                       sm_scale, out, lse, workspace), _stream(stream))
     _check(rc, "ddtree_verify_mla_batched")
 
 
@@ -210,15 +255,10 @@ def ddtree_verify_mla_batched_timed(plan: Plan, q_latent, q_rope, kv_pool, kv_in
                                     stage_events, stream=None) -> None:
     """As ddtree_verify_mla_batched, recording three torch.cuda.Event objects
     (before the partial kernel, between partial and combine, after combine)."""
-    bf, i32 = torch.bfloat16, torch.int32
     evs = (ctypes.c_void_p * 3)(*[None if e is None else e.cuda_event for e in stage_events])
     rc = library().ddtree_verify_mla_batched_timed(
-        ctypes.byref(plan), _dev(q_latent, bf, "q_latent"), _dev(q_rope, bf, "q_rope"),
-        _dev(kv_pool, bf, "kv_pool"), _dev(kv_indices, i32, "kv_indices"),
-        _dev(kv_indptr, i32, "kv_indptr"), _dev(prefix_lens, i32, "prefix_lens"),
-        _dev(tree_parent, i32, "tree_parent"), float(sm_scale), _dev(out, bf, "out"),
-        _dev(lse, torch.float32, "lse"), _dev(workspace, torch.uint8, "workspace"),
-        workspace.numel(), _stream(stream), ctypes.cast(evs, ctypes.c_void_p))
+        *_batched_args(plan, q_latent, q_rope, kv_pool, kv_indices, kv_indptr, prefix_lens, tree_parent,
+                       sm_scale, out, lse, workspace), _stream(stream), ctypes.cast(evs, ctypes.c_void_p))
     _check(rc, "ddtree_verify_mla_batched_timed")
 
 

@@ -74,6 +74,10 @@ int choose_kernel(int kernel, int rows_per_req, int64_t total_keys) {
   return rows_per_req > 128 ? DDTREE_KERNEL_TC2 : DDTREE_KERNEL_TC;
 }
 
+// Bytes of one split's partial O rows (bf16) and LSEs (fp32).
+inline int64_t partial_o_bytes(int64_t splits, int64_t rows) { return round_up(splits * rows * kLatent * 2, 256); }
+inline int64_t partial_lse_bytes(int64_t splits, int64_t rows) { return round_up(splits * rows * 4, 256); }
+
 // SMs the chosen kernel can keep busy at once on the current device.  A
 // tensor-core work item is a cluster, and clusters are placed within one GPC,
 // so a GPC whose SM count is not a multiple of the cluster size leaves SMs
@@ -129,6 +133,7 @@ extern "C" int ddtree_verify_mla_plan_ex(int batch, int n_nodes, int n_heads,
   p.pool_rows = pool_rows;
   p.max_keys = (int32_t)max_keys;
   p.kernel = choose_kernel(kernel, p.rows_per_req, total_keys);
+  const bool device_sized = num_sms == 0;
   if (num_sms == 0) {
     int rc = usable_sms(p.kernel, &num_sms);
     if (rc != DDTREE_OK) return rc;
@@ -139,32 +144,53 @@ extern "C" int ddtree_verify_mla_plan_ex(int batch, int n_nodes, int n_heads,
   p.tile_keys = g.tile_keys;
   p.row_tiles = (p.rows_per_req + g.row_tile - 1) / g.row_tile;
 
-  // Split rule: enough work items (row tile x key chunk) for `waves` CTAs
-  // per SM, with chunks a whole number of tiles.  A tensor-core work item is
-  // a cluster of two CTAs (scorer + accumulator), so it occupies two SMs.
-  // The pair form is a cluster of four CTAs covering two row tiles.
+  // Split rule ("Chunk 66.1": the split count decides whether the SMs are
+  // fed).  A work item is one row group x one key chunk; chunks are a whole
+  // number of tiles.  A tensor-core work item is a cluster (2 CTAs for the
+  // pair kernel, 4 for the cluster-of-four kernel covering two row tiles),
+  // and the clusters the device holds at once make one wave.  The cluster
+  // kernels take the shortest chunk whose work items -- counted after each
+  // request's own rounding -- fit one wave; the CUDA-core kernel aims at a
+  // few CTAs per SM.
   const int64_t ctas_per_item = p.kernel == DDTREE_KERNEL_TC2 ? 4 : (p.kernel == DDTREE_KERNEL_TC ? 2 : 1);
   const int64_t row_groups = p.kernel == DDTREE_KERNEL_TC2 ? (p.row_tiles + 1) / 2 : p.row_tiles;
-  int64_t target_items = (int64_t)g.waves * num_sms / ctas_per_item;
-  int64_t target_splits = std::max<int64_t>(1, (target_items + row_groups - 1) / row_groups);
-  int64_t chunk = (total_keys + target_splits - 1) / target_splits;
-  chunk = round_up(std::max<int64_t>(chunk, g.tile_keys), g.tile_keys);
-  chunk = std::min<int64_t>(chunk, round_up(max_keys, g.tile_keys));
+  const int64_t target_items = std::max<int64_t>(1, (int64_t)g.waves * num_sms / ctas_per_item);
+  auto items_for = [&](int64_t chunk) {
+    int64_t n = 0;
+    for (int b = 0; b < batch; ++b) n += ((int64_t)prefix_lens_host[b] + n_nodes + chunk - 1) / chunk;
+    return n * row_groups;
+  };
+  const int64_t chunk_max = round_up(max_keys, g.tile_keys);
+  int64_t chunk;
+  if (p.kernel == DDTREE_KERNEL_SIMT) {
+    const int64_t target_splits = std::max<int64_t>(1, (target_items + row_groups - 1) / row_groups);
+    chunk = round_up(std::max<int64_t>((total_keys + target_splits - 1) / target_splits, g.tile_keys), g.tile_keys);
+    chunk = std::min<int64_t>(chunk, chunk_max);
+  } else {
+    // Smallest k with items_for(k tiles) <= target (items fall as k grows).
+    int64_t lo = 1, hi = chunk_max / g.tile_keys;
+    while (lo < hi) {
+      const int64_t mid = lo + (hi - lo) / 2;
+      if (items_for(mid * g.tile_keys) <= target_items) hi = mid;
+      else lo = mid + 1;
+    }
+    chunk = lo * g.tile_keys;
+  }
   if (const char* env = getenv("DDTREE_CHUNK_KEYS")) {
     long v = strtol(env, nullptr, 10);
     if (v > 0) chunk = round_up(v, g.tile_keys);
   }
   p.chunk_keys = (int32_t)chunk;
-  int64_t splits = 0;
-  for (int b = 0; b < batch; ++b) splits += ((int64_t)prefix_lens_host[b] + n_nodes + chunk - 1) / chunk;
+  const int64_t splits = items_for(chunk) / row_groups;
   if (splits > INT32_MAX / 4) return DDTREE_EINVAL;
   p.total_splits = (int32_t)splits;
+  // The cluster-of-four kernel merges the splits itself (no second launch)
+  // when all of its clusters are resident at once on this device.
+  p.fused_combine = (p.kernel == DDTREE_KERNEL_TC2 && device_sized && items_for(chunk) <= target_items) ? 1 : 0;
 
   p.off_partial_lse = kStatusBytes;
-  int64_t lse_bytes = round_up(splits * p.rows_per_req * 4, 256);
-  p.off_partial_o = p.off_partial_lse + lse_bytes;
-  int64_t o_bytes = round_up(splits * p.rows_per_req * (int64_t)kLatent * 4, 256);
-  p.workspace_bytes = p.off_partial_o + o_bytes;
+  p.off_partial_o = p.off_partial_lse + partial_lse_bytes(splits, p.rows_per_req);
+  p.workspace_bytes = p.off_partial_o + partial_o_bytes(splits, p.rows_per_req);
   *plan = p;
   return DDTREE_OK;
 }
@@ -195,11 +221,13 @@ int validate_plan(const ddtree_plan_t* p) {
   if (p->row_tiles != (p->rows_per_req + g.row_tile - 1) / g.row_tile) return DDTREE_EINVAL;
   if (p->chunk_keys < p->tile_keys || p->chunk_keys % p->tile_keys) return DDTREE_EINVAL;
   if (p->total_splits < p->batch) return DDTREE_EINVAL;
-  int64_t lse_bytes = round_up((int64_t)p->total_splits * p->rows_per_req * 4, 256);
-  int64_t o_bytes = round_up((int64_t)p->total_splits * p->rows_per_req * (int64_t)kLatent * 4, 256);
+  const int64_t lse_bytes = partial_lse_bytes(p->total_splits, p->rows_per_req);
+  const int64_t o_bytes = partial_o_bytes(p->total_splits, p->rows_per_req);
   if (p->off_partial_lse != kStatusBytes || p->off_partial_o != kStatusBytes + lse_bytes ||
       p->workspace_bytes != p->off_partial_o + o_bytes)
     return DDTREE_EINVAL;
+  if (p->fused_combine != 0 && (p->fused_combine != 1 || p->kernel != DDTREE_KERNEL_TC2)) return DDTREE_EINVAL;
+  if (p->wait_limit_us < 0) return DDTREE_EINVAL;
   int ls = p->q_latent_row_stride, rs = p->q_rope_row_stride;
   if (ls != 0 && (ls < kLatent || ls % 8)) return DDTREE_EINVAL;
   if (rs != 0 && (rs < kRope || rs % 8)) return DDTREE_EINVAL;
@@ -238,8 +266,11 @@ int run(const ddtree_plan_t* p, const uint16_t* q_latent, const uint16_t* q_rope
   a.lse = lse;
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   a.status = reinterpret_cast<uint32_t*>(ws);
+  a.grid_done = reinterpret_cast<uint32_t*>(ws + 8);
   a.partial_lse = reinterpret_cast<float*>(ws + p->off_partial_lse);
-  a.partial_o = reinterpret_cast<float*>(ws + p->off_partial_o);
+  a.partial_o = reinterpret_cast<uint16_t*>(ws + p->off_partial_o);
+  a.fused = p->fused_combine;
+  a.wait_ns = p->wait_limit_us > 0 ? (uint64_t)p->wait_limit_us * 1000ull : 2000000000ull;
   a.pool_rows = p->pool_rows;
   a.sm_scale = sm_scale;
   a.batch = p->batch;
@@ -265,7 +296,7 @@ int run(const ddtree_plan_t* p, const uint16_t* q_latent, const uint16_t* q_rope
         : (p->kernel == DDTREE_KERNEL_TC) ? launch_partial_tc(a, stream)
                                           : launch_partial_simt(a, stream);
   if (e == cudaSuccess && ev && ev[1]) e = record_event(ev[1], stream);
-  if (e == cudaSuccess) e = launch_combine(a, stream);
+  if (e == cudaSuccess && !a.fused) e = launch_combine(a, stream);
   if (e == cudaSuccess && ev && ev[2]) e = record_event(ev[2], stream);
   if (e != cudaSuccess) {
     cudaGetLastError();

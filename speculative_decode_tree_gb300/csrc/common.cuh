@@ -28,14 +28,17 @@ struct VerifyArgs {
   uint16_t* out;
   float* lse;
   float* partial_lse;          // [total_splits, rows_per_req]
-  float* partial_o;            // [total_splits, rows_per_req, 512]
+  uint16_t* partial_o;         // [total_splits, rows_per_req, 512] bf16
   uint32_t* status;            // workspace offset 0
+  uint32_t* grid_done;         // workspace offset 8: CTAs finished (fused combine)
   int64_t pool_rows;           // <= 0: indices unchecked
   float sm_scale;
   int32_t prefix_len_host;
   int32_t batch, n_nodes, n_heads, rows_per_req;
   int32_t tile_keys, chunk_keys, total_splits, row_tile, row_tiles;
   int32_t q_lat_stride, q_rope_stride;
+  int32_t fused;               // the partial kernel merges the splits itself
+  uint64_t wait_ns;            // bound of every wait inside the kernels
 };
 
 // One work item's request: which request a split slot belongs to, and the
@@ -60,12 +63,12 @@ __device__ __forceinline__ bool locate_split(const VerifyArgs& a, int w, SplitLo
   int acc = 0;
   for (int r = 0; r < a.batch; ++r) {
     int P = dev_prefix_len(a, r);
-    if (P < 0) {
+    if (P < 0 || P > INT32_MAX - 2 * DDTREE_MAX_NODES) {
       atomicOr(a.status, DDTREE_ST_BAD_LENGTH);
       return false;
     }
     int n = P + a.n_nodes;
-    int ns = (n + a.chunk_keys - 1) / a.chunk_keys;
+    int ns = (int)(((int64_t)n + a.chunk_keys - 1) / a.chunk_keys);
     if (w < acc + ns) {
       loc.b = r;
       loc.s = w - acc;
@@ -88,15 +91,17 @@ __device__ __forceinline__ bool locate_split(const VerifyArgs& a, int w, SplitLo
 }
 
 // First slot and split count of request b (for the combine stage).
+// Split counts are taken in 64 bits: P + T + chunk can pass INT32_MAX when
+// one split covers nearly all keys.
 __device__ __forceinline__ void request_slots(const VerifyArgs& a, int b, int& first, int& count) {
-  int acc = 0;
+  int64_t acc = 0;
   for (int r = 0; r < b; ++r) {
-    int P = max(dev_prefix_len(a, r), 0);
+    const int64_t P = max(dev_prefix_len(a, r), 0);
     acc += (P + a.n_nodes + a.chunk_keys - 1) / a.chunk_keys;
   }
-  int P = max(dev_prefix_len(a, b), 0);
-  first = acc;
-  count = (P + a.n_nodes + a.chunk_keys - 1) / a.chunk_keys;
+  const int64_t P = max(dev_prefix_len(a, b), 0);
+  first = (int)(acc < (int64_t)INT32_MAX ? acc : (int64_t)INT32_MAX);
+  count = (int)((P + a.n_nodes + a.chunk_keys - 1) / a.chunk_keys);
 }
 
 // Ancestor set of node i as a bitmask: bit j set when j is i or one of its

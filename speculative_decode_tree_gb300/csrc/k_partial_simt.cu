@@ -173,7 +173,7 @@ __global__ void __launch_bounds__(kThreads) partial_simt_kernel(const VerifyArgs
     sL[tid] = l_run;
   }
   __syncthreads();
-  float* po = a.partial_o + (size_t)slot * a.rows_per_req * kLatent;
+  uint16_t* po = a.partial_o + (size_t)slot * a.rows_per_req * kLatent;
   float* pl = a.partial_lse + (size_t)slot * a.rows_per_req;
 #pragma unroll
   for (int r = 0; r < SR; ++r) {
@@ -181,8 +181,8 @@ __global__ void __launch_bounds__(kThreads) partial_simt_kernel(const VerifyArgs
     if (row >= a.rows_per_req) break;
     float l = sL[r];
     float inv = l > 0.f ? 1.f / l : 0.f;
-    *reinterpret_cast<float2*>(po + (size_t)row * kLatent + d0) =
-        make_float2(acc[r][0] * inv, acc[r][1] * inv);
+    *reinterpret_cast<__nv_bfloat162*>(po + (size_t)row * kLatent + d0) =
+        __floats2bfloat162_rn(acc[r][0] * inv, acc[r][1] * inv);
     if (tid == 0) pl[row] = l > 0.f ? sM[r] + logf(l) : -INFINITY;
   }
 }

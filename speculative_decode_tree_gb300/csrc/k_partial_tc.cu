@@ -549,7 +549,7 @@ __device__ void accumulator(const VerifyArgs& a, const PoolMaps& maps, const Ite
                      : "memory");
       if (stop) break;
     }
-    // Epilogue: O_s = O / l, written as fp32 rows of the workspace.
+    // Epilogue: O_s = O / l, written as bf16 rows of the workspace.
     const bool done = wait_or_abort(&c->mma_done, 0, c, a.status);
     tc_fence_after();
     const int req_row = it.row0 + r;
@@ -558,21 +558,24 @@ __device__ void accumulator(const VerifyArgs& a, const PoolMaps& maps, const Ite
     // the abort flag); the TMEM loads are warp-collective, the stores per row.
     if (__all_sync(0xffffffffu, done)) {
       const float inv = lfin > 0.f ? 1.f / lfin : 0.f;
-      float* po = a.partial_o + ((size_t)it.slot * a.rows_per_req + (row_ok ? req_row : 0)) * kLatent;
+      uint16_t* po = a.partial_o + ((size_t)it.slot * a.rows_per_req + (row_ok ? req_row : 0)) * kLatent;
       uint32_t v[16];
       for (int q = 0; q < 32; ++q) {
         tmem_ld16(lane_addr + 16 * q, v);
         if (row_ok) {
+          uint32_t pk[8];
 #pragma unroll
-          for (int e = 0; e < 16; e += 4)
-            *reinterpret_cast<float4*>(po + 16 * q + e) =
-                make_float4(__uint_as_float(v[e]) * inv, __uint_as_float(v[e + 1]) * inv,
-                            __uint_as_float(v[e + 2]) * inv, __uint_as_float(v[e + 3]) * inv);
+          for (int e = 0; e < 8; ++e) {
+            __nv_bfloat162 b2 = __floats2bfloat162_rn(__uint_as_float(v[2 * e]) * inv, __uint_as_float(v[2 * e + 1]) * inv);
+            pk[e] = *reinterpret_cast<uint32_t*>(&b2);
+          }
+          *reinterpret_cast<uint4*>(po + 16 * q) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+          *reinterpret_cast<uint4*>(po + 16 * q + 8) = make_uint4(pk[4], pk[5], pk[6], pk[7]);
         }
       }
     } else if (row_ok) {
       for (int d = 0; d < kLatent; ++d)
-        a.partial_o[((size_t)it.slot * a.rows_per_req + req_row) * kLatent + d] = 0.f;
+        a.partial_o[((size_t)it.slot * a.rows_per_req + req_row) * kLatent + d] = 0;
     }
   }
 }

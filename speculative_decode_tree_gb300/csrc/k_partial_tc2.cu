@@ -16,20 +16,28 @@
 // 2+c loads value chunks 2q+c (64 of the 512 columns) of all 128 keys.
 //
 // Scorer CTA: Q latent (128 x 512 bf16) in TMEM (A operand), Q rope in shared
-// memory; S tiles (128 rows x 128 keys, fp32) double-buffered in TMEM; four
-// softmax warps (one query row per thread) mask tree keys against the
-// ancestor bits, keep a lazily rescaled running max and write P (bf16,
-// K-major, 128-byte swizzle) plus per-row rescale factors, shipped to the
-// same-row-tile accumulator by a bulk shared-memory copy across the cluster.
+// memory; S tiles (128 rows x 128 keys, fp32) double-buffered in TMEM; two
+// softmax warpgroups (one query row per thread, 64 keys each) mask tree keys
+// against the ancestor bits, agree on a lazily rescaled running max and write
+// P (bf16, K-major, 128-byte swizzle) plus per-row rescale factors, shipped
+// to the same-row-tile accumulator by a bulk shared-memory copy.
 // Accumulator CTA: O (128 x 512 fp32) in all 512 TMEM columns; its epilogue
 // warps rescale O rows when the running max moved (rare) and finally write
 // O_s = O / l; the scorer writes lse_s.
 //
-// Gathers: 16-byte cp.async of the scattered 1152-byte rows through the
-// page_size=1 index table ("Chunk 66.1": 128-bit KV loads) into 128-byte
-// swizzled chunks; a tile whose 128 indices form one contiguous run uses 2-D
-// TMA tile loads instead.  The follower CTA of each pair forwards "my half
-// landed" to the leader, whose MMA thread waits for both halves.
+// Gathers ("Chunk 66.1": 128-bit KV loads): the work item's indices pass
+// through a shared-memory ring filled ahead by a loader warp (which, in the
+// accumulator CTAs, also pulls every key row into L2 a ring's length ahead).
+// Load/store-unit warps copy most 64-column chunks of the scattered 1152-byte
+// rows with 16-byte cp.async while TMA warps fetch the remaining chunks with
+// gather4 loads at the same time, so both paths into shared memory are busy
+// at once; a tile whose 128 indices form one contiguous run comes by 2-D TMA
+// tile loads instead.  A TMA warp's loads complete on its own barriers (one
+// lane issues, another lane waits for each tile's bytes and then counts the
+// warp in), so every load a CTA issued is known to have landed before it
+// exits, also after an expired wait.  The follower CTA of each pair forwards
+// "my tile is complete" to the leader, whose MMA thread then issues the
+// tile's MMAs back to back.
 //
 // Every mbarrier wait is bounded; on expiry the kernel sets
 // DDTREE_ST_TIMEOUT, stops issuing work, waits (bounded) for its own
@@ -37,6 +45,7 @@
 #include <cuda.h>
 #include <string.h>
 
+#include "combine.cuh"
 #include "common.cuh"
 #include "tc_ptx.cuh"
 
@@ -50,51 +59,64 @@ constexpr int ROWS = 128;                // query rows per CTA
 constexpr int HALF = 64;                 // keys per scorer CTA per tile
 constexpr int SCHUNK = HALF * 128;       // scorer chunk: 64 keys x 64 columns (8 KB)
 constexpr int VCHUNK = TK * 128;         // accumulator chunk: 128 keys x 64 columns (16 KB)
-// The key rings are rings of units of several chunks with one mbarrier per
-// unit: a producer warp signals a unit with one cp.async-tracked arrive, which
-// keeps more bytes in flight per arrive than a barrier per chunk.
-constexpr int QU = 3;                    // scorer chunks per unit (24 KB)
-constexpr int QUNITS = 7;                // scorer unit slots (2.3 tiles)
-constexpr int QUNIT_BYTES = QU * SCHUNK;
-constexpr int VU = 2;                    // accumulator chunks per unit (32 KB)
-constexpr int VUNITS = 4;                // accumulator unit slots (2 tiles)
-constexpr int VUNIT_BYTES = VU * VCHUNK;
+// Rings of two tiles.  Scorer slot: the 9 chunks of its 64 keys (chunk c at
+// c x 8 KB; chunks 0..5 by cp.async, 6..8 by TMA).  Accumulator slot: its 4
+// value chunks of all 128 keys (chunk q = columns 64 (2q+p) .. at q x 16 KB;
+// q = 0..2 by cp.async, q = 3 by TMA).
+constexpr int KSLOT = 9 * SCHUNK;        // 72 KB
+constexpr int VSLOT = 4 * VCHUNK;        // 64 KB
+constexpr int kScorerLsuChunks = 6;
+constexpr int kAccLsuChunks = 3;
 constexpr int PTILE = 32768;             // bf16 P tile: 2 swizzle atoms of 128 rows x 128 B
-constexpr int META = 1040;               // alpha[128], lfin[128], flag words[4]
+constexpr int META = 1552;               // alpha[128], l0[128], l1[128], flag words[4]
 constexpr int PCOPY = PTILE + META;      // bytes shipped per tile (multiple of 16)
 constexpr int PBUF = 34816;              // P buffer stride (1024-aligned)
-constexpr int kThreads = 384;            // 12 warps
-constexpr int kScorerProducers = 7;      // warps 0, 2, 3, 8..11
-constexpr int kAccProducers = 6;         // warps 0, 3, 8..11
-constexpr int kScorerLsuChunks = 6;      // scorer chunks 0..5 by cp.async, 6..8 by TMA gather4
-constexpr int kAccLsuChunks = 3;         // accumulator chunks q = 0..2 by cp.async, q = 3 by TMA gather4
+constexpr int NIDX = 8;                  // index ring: tiles of indices held ahead
+constexpr int kThreads = 512;            // 16 warps
+constexpr int kLsuWarps = 4;             // producer warps on the load/store unit (cp.async)
+constexpr int kTmaWarps = 2;             // producer warps issuing TMA loads
+constexpr int kLoaderWarp = 15;
 constexpr float kLazyRescale = 8.0f;     // rescale only when the max grows by > 2^8 (log2 units)
-constexpr uint64_t kWaitNs = 2000000000ull;
-constexpr uint16_t kScorerPair = 0x3, kAccPair = 0xC;
+// Tensor-core work must be complete before TMEM is freed: this wait keeps a
+// fixed bound whatever the caller's limit.
+constexpr uint64_t kDrainNs = 2000000000ull;
+constexpr uint16_t kScorerPair = 0x3, kAccPair = 0xC, kAllFour = 0xF;
 
 // Shared-memory map (offsets from a 1024-aligned base).
-constexpr int Q_ROPE = 0;                          // scorer: 16 KB
-constexpr int Q_RING = Q_ROPE + VCHUNK;            // scorer: 7 x 24 KB
-constexpr int Q_STAGE = Q_RING + QUNITS * QUNIT_BYTES;  // scorer: P staging
+constexpr int Q_ROPE = 0;                               // scorer: 16 KB
+constexpr int Q_RING = Q_ROPE + VCHUNK;                 // scorer: 2 x 72 KB
+constexpr int Q_STAGE = Q_RING + 2 * KSLOT;             // scorer: P staging
 constexpr int Q_END = Q_STAGE + PBUF;
-constexpr int V_PBUF = 0;                          // accumulator: 2 x PBUF
-constexpr int V_RING = V_PBUF + 2 * PBUF;          // accumulator: 8 x 16 KB
-constexpr int V_END = V_RING + VUNITS * VUNIT_BYTES;
-constexpr int BIG_END = (Q_END > V_END ? Q_END : V_END);
+constexpr int V_PBUF = 0;                               // accumulator: 2 x PBUF
+constexpr int V_RING = V_PBUF + 2 * PBUF;               // accumulator: 2 x 64 KB
+constexpr int V_END = V_RING + 2 * VSLOT;
+constexpr int IDX_RING = (Q_END > V_END ? Q_END : V_END);  // both: NIDX x 128 int32
+constexpr int BIG_END = IDX_RING + NIDX * TK * 4;
+
 
 struct __align__(8) Ctrl {
+  // Ring slot barriers (per tile slot): full = this CTA's chunks of the tile
+  // landed (every producer lane + each TMA warp once), peer = (leader) the
+  // follower's slot is full, empty = the pair's MMAs consumed the slot
+  // (commit multicast to both CTAs of the pair); tma = each TMA warp's own
+  // loads of the tile landed.
+  uint64_t full[2], peer[2], empty[2], tma[kTmaWarps][2];
+  uint32_t tma_issued[kTmaWarps];  // tiles whose TMA loads a warp has issued
   // scorer
-  uint64_t kfull[QUNITS], kpeer[QUNITS], kempty[QUNITS];
   uint64_t sfull[2], sempty[2], pfree[2];
   // accumulator
-  uint64_t vfull[VUNITS], vpeer[VUNITS], vempty[VUNITS];
   uint64_t pfull[2], ppeer[2], pvdone[2], corr_done[2];
   // both
+  uint64_t ifull[NIDX], iempty[NIDX];  // index ring
+  int32_t ifirst[NIDX];    // first index of each ring tile
+  int32_t icontig[NIDX];   // the tile's 128 indices form one run
   uint64_t mma_done;
   uint64_t q_ready;   // scorer: Q latent in TMEM and Q rope in shared memory
+  uint64_t wait_ns;        // bound of the waits (the caller's, default 2 s)
   uint32_t tmem_base;
   uint32_t abort;
-  uint32_t key_mask[2][4];
+  float xmax[2][128];      // scorer: per-row maxima / sums exchanged between the softmax halves
+  uint32_t merge_zero;     // fused merge: the partials cannot be trusted (a wait timed out)
   uint64_t anc[64];
   int32_t par[64];   // the request's parents, staged for the ancestor walk
 };
@@ -112,11 +134,28 @@ __device__ __forceinline__ void set_abort(Ctrl* c, uint32_t* status) {
 // on expiry mark the CTA aborted.  False when aborted.
 __device__ __forceinline__ bool wait_clu(uint64_t* bar, uint32_t parity, Ctrl* c, uint32_t* status) {
   if (aborted(c)) return false;
-  if (mbar_wait_cluster(bar, parity, global_timer_ns() + kWaitNs)) return true;
+  if (mbar_wait_cluster(bar, parity, global_timer_ns() + c->wait_ns)) return true;
   set_abort(c, status);
   return false;
 }
-__device__ __forceinline__ void remote_arrive(uint32_t remote_bar) {
+// Same, CTA scope (barriers arrived on by this CTA's own threads).
+__device__ __forceinline__ bool wait_cta(uint64_t* bar, uint32_t parity, Ctrl* c, uint32_t* status) {
+  if (aborted(c)) return false;
+  if (mbar_wait(bar, parity, global_timer_ns() + c->wait_ns)) return true;
+  set_abort(c, status);
+  return false;
+}
+// Arrive on a barrier in another CTA of the cluster.  Relaxed: a pure
+// signal.  Every use orders what it must by other means (the data it
+// announces was itself completed through an mbarrier, or is a register value
+// already consumed).  Under a load of in-flight copies a cluster-scope
+// release here cost up to ~1.5 us per arrive.
+__device__ __forceinline__ void signal_remote(uint32_t remote_bar) {
+  asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(remote_bar) : "memory");
+}
+// Arrive with cluster-scope release: the arriving thread's earlier shared-
+// memory reads must be complete before the remote side reuses the memory.
+__device__ __forceinline__ void release_remote(uint32_t remote_bar) {
   asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(remote_bar) : "memory");
 }
 __device__ __forceinline__ void named_bar(int id, int nthreads) {
@@ -137,9 +176,7 @@ __device__ __forceinline__ bool named_bar_or(int id, int nthreads, bool pred) {
 // ---- cta_group::2 tensor-core instructions (issued by the pair's even CTA)
 // Four K steps (K = 16 each) of one 64-column chunk per statement, the
 // operand addresses stepped inside PTX.  One MMA of M = 256, N = 128 is 64
-// tensor cycles per SM, so the issue path must stay short: with one statement
-// and C++ descriptor arithmetic per MMA the pipe ran at about 55 % on the
-// 65k-prefix workload, which this form lifts by ~6 us per call.
+// tensor cycles per SM, so the issue path must stay short.
 // A from TMEM (row r in lane r, 8 columns = 16 bf16 per K step), B by
 // descriptor (K-major, 128-byte swizzle: 32 bytes per K step).
 __device__ __forceinline__ void mma2_ts_x4(uint32_t d, uint32_t a0, uint64_t b0, uint32_t idesc,
@@ -196,151 +233,150 @@ struct Item {
 struct PoolMaps {
   CUtensorMap half;   // 64 columns x 64 rows box: a scorer's half of a contiguous tile
   CUtensorMap tile;   // 64 columns x 128 rows box: an accumulator chunk of a contiguous tile
-  CUtensorMap po;     // partial O [splits][rows_per_req][512] fp32, 32 columns x 128 rows box
   CUtensorMap row;    // 64 columns x 1 row box: four scattered rows per gather4 load
+  CUtensorMap po;     // partial O [splits][rows_per_req][512] bf16, 64 columns x 128 rows box
 };
 
-// One tile's 128 indices: lane l holds keys 4l .. 4l+3 (-1 past the chunk or
-// outside the pool); the raw loads are issued a tile early.
-struct RawIdx {
-  int v[4];
-};
-struct TileIdx {
-  int4 k4;
-  int first;
-  bool contiguous;
-};
-__device__ __forceinline__ RawIdx raw_tile_indices(const VerifyArgs& a, const Item& it, int tile, int lane) {
-  const int k0 = it.k_begin + tile * TK + 4 * lane;
-  RawIdx r;
-#pragma unroll
-  for (int j = 0; j < 4; ++j) r.v[j] = (k0 + j < it.k_end) ? __ldg(a.kv_indices + it.loc.idx_base + k0 + j) : -1;
-  return r;
-}
-__device__ __forceinline__ TileIdx finish_tile_indices(const VerifyArgs& a, RawIdx r, int lane) {
-#pragma unroll
-  for (int j = 0; j < 4; ++j)
-    if (r.v[j] < 0 || (a.pool_rows > 0 && r.v[j] >= a.pool_rows)) r.v[j] = -1;
-  TileIdx t;
-  t.k4 = make_int4(r.v[0], r.v[1], r.v[2], r.v[3]);
-  t.first = __shfl_sync(0xffffffffu, r.v[0], 0);
-  const bool run = r.v[0] >= 0 && r.v[0] == t.first + 4 * lane && r.v[1] == r.v[0] + 1 &&
-                   r.v[2] == r.v[0] + 2 && r.v[3] == r.v[0] + 3;
-  t.contiguous = __all_sync(0xffffffffu, run);
-  return t;
+// ------------------------------------------------------------ index ring
+__device__ __forceinline__ int* ring_tile(uint8_t* sm, int t) {
+  return reinterpret_cast<int*>(sm + IDX_RING) + (t % NIDX) * TK;
 }
 
-// Index of key (4 g + lane/8) of the groups this producer lane copies: a
-// contiguous block of groups g = first .. first+n-1 (of ngroups, split as
-// evenly as the np producer warps allow), taken from the lane that holds them
-// (tile key 4 (g0 + g) + lane/8, g0 = first group of this CTA's keys).
-struct MyKeys {
-  int id[6];
-  int n;
-  int first;
-};
-__device__ __forceinline__ MyKeys my_keys(const TileIdx& ti, int lane, int rank, int np, int g0, int ngroups) {
-  MyKeys mk;
-  const int per = ngroups / np, extra = ngroups % np;
-  mk.first = rank * per + min(rank, extra);
-  mk.n = per + (rank < extra ? 1 : 0);
-  const int sel = lane >> 3;
+// Loader warp: tile j's 128 indices (invalid ones -> -1, flagged) into ring
+// slot j % NIDX, with the tile's first index and whether it is one run; in
+// the accumulator CTAs each valid row is also pulled into L2 right away,
+// NIDX tiles ahead of the slowest consumer.
+__device__ void index_loader(const VerifyArgs& a, const Item& it, uint8_t* sm, Ctrl* c, bool prefetch) {
+  const int lane = threadIdx.x & 31;
+  for (int j = 0; j < it.ntiles; ++j) {
+    const int slot = j % NIDX;
+    if (j >= NIDX && !wait_cta(&c->iempty[slot], ((j / NIDX) - 1) & 1, c, a.status)) return;
+    const int k0 = it.k_begin + j * TK + 4 * lane;
+    int v[4];
 #pragma unroll
-  for (int j = 0; j < 6; ++j) {
-    const int g = mk.first + j;
-    const int src = (g0 + g) & 31;
-    const int x = __shfl_sync(0xffffffffu, ti.k4.x, src);
-    const int y = __shfl_sync(0xffffffffu, ti.k4.y, src);
-    const int z = __shfl_sync(0xffffffffu, ti.k4.z, src);
-    const int w = __shfl_sync(0xffffffffu, ti.k4.w, src);
-    mk.id[j] = sel == 0 ? x : sel == 1 ? y : sel == 2 ? z : w;
-  }
-  return mk;
-}
-
-// Fills one 64-column chunk (columns 64*col_chunk ..) of `nkeys` key rows
-// (tile keys key0 .. key0+nkeys-1) into `dst` (row k at dst + 128 k,
-// 128-byte swizzled).  TMA bytes are expected on `bar`; the caller arrives
-// on it once per lane after the last chunk of a unit.  Scattered rows come
-// by 16-byte cp.async (load/store unit) or, when `g4` is set, by TMA gather4
-// loads of four rows each: the TMA engine is a second path into shared
-// memory, so giving it some of the chunks raises a CTA's gather rate.
-__device__ __forceinline__ void fill_chunk(const PoolMaps& maps, const uint16_t* pool, uint8_t* dst, int col_chunk,
-                                           int key0, int nkeys, const TileIdx& ti, const MyKeys& mk, int rank,
-                                           int lane, uint64_t* bar, bool g4) {
-  if (ti.contiguous) {
-    if (rank == 0 && lane == 0) {
-      mbar_expect_tx(bar, nkeys * 128);
-      asm volatile(
-          "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];"
-          ::"r"(smem_u32(dst)), "l"(nkeys == TK ? &maps.tile : &maps.half), "r"(col_chunk * 64),
-            "r"(ti.first + key0), "r"(smem_u32(bar))
-          : "memory");
-    }
-    __syncwarp();
-  } else if (g4) {
-    if (lane == 0 && mk.n > 0) mbar_expect_tx(bar, mk.n * 512);
+    for (int e = 0; e < 4; ++e) v[e] = (k0 + e < it.k_end) ? __ldg(a.kv_indices + it.loc.idx_base + k0 + e) : -1;
 #pragma unroll
-    for (int j = 0; j < 6; ++j) {
-      if (j < mk.n) {  // warp-uniform
-        // Rows of group first+j are held by lanes 0, 8, 16, 24; a missing
-        // key (-1) reads row 0 instead: its score is masked and its weight is 0.
-        const int r0 = max(mk.id[j], 0);
-        const int r1 = max(__shfl_sync(0xffffffffu, mk.id[j], 8), 0);
-        const int r2 = max(__shfl_sync(0xffffffffu, mk.id[j], 16), 0);
-        const int r3 = max(__shfl_sync(0xffffffffu, mk.id[j], 24), 0);
-        if (lane == 0)
-          asm volatile(
-              "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes"
-              " [%0], [%1, {%2, %3, %4, %5, %6}], [%7];" ::"r"(smem_u32(dst + 4 * (mk.first + j) * 128)),
-              "l"(&maps.row), "r"(col_chunk * 64), "r"(r0), "r"(r1), "r"(r2), "r"(r3), "r"(smem_u32(bar))
-              : "memory");
+    for (int e = 0; e < 4; ++e) {
+      if (k0 + e < it.k_end && (v[e] < 0 || (a.pool_rows > 0 && v[e] >= a.pool_rows))) {
+        atomicOr(a.status, DDTREE_ST_BAD_INDEX);
+        v[e] = -1;
       }
     }
+    int* dst = ring_tile(sm, j);
+    *reinterpret_cast<int4*>(dst + 4 * lane) = make_int4(v[0], v[1], v[2], v[3]);
+    const int first = __shfl_sync(0xffffffffu, v[0], 0);
+    const bool run = v[0] >= 0 && v[0] == first + 4 * lane && v[1] == v[0] + 1 && v[2] == v[0] + 2 &&
+                     v[3] == v[0] + 3;
+    const bool contig = __all_sync(0xffffffffu, run);
+    if (lane == 0) {
+      c->ifirst[slot] = first;
+      c->icontig[slot] = contig ? 1 : 0;
+    }
     __syncwarp();
-  } else {
-    const int piece = lane & 7;
-    const uint32_t base = smem_u32(dst);
+    mbar_arrive(&c->ifull[slot]);  // 32 arrivals: every lane's stores are released
+    if (prefetch) {
 #pragma unroll
-    for (int j = 0; j < 6; ++j) {
-      if (j < mk.n) {
-        const int row = 4 * (mk.first + j) + (lane >> 3);  // row within this chunk
-        const int id = mk.id[j];
-        const uint16_t* src = pool + (size_t)(id < 0 ? 0 : id) * kRow + col_chunk * 64 + piece * 8;
-        cp_async16_zfill(base + row * 128 + ((piece ^ (row & 7)) << 4), src, id < 0 ? 0u : 16u);
-      }
+      for (int e = 0; e < 4; ++e)
+        if (v[e] >= 0)
+          asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(a.kv_pool + (size_t)v[e] * kRow),
+                       "r"(kRow * 2)
+                       : "memory");
     }
   }
 }
 
-// Pulls whole 1152-byte key rows of a tile into L2 (one bulk prefetch per
-// row, from the accumulator's otherwise idle TMA unit); thread r -> key r.
-// Eight tiles ahead of the accumulator (about six ahead of the scorer's
-// gathers) measured best on the 65k-prefix and mixed-batch workloads: 3
-// tiles ahead cost 2 us per call more, 16 (the whole chunk up front) 5 us.
-constexpr int kL2Ahead = 8;
-__device__ __forceinline__ void prefetch_tile_l2(const VerifyArgs& a, const Item& it, int tile, int r) {
-  if (tile >= it.ntiles) return;
-  const int kp = it.k_begin + tile * TK + r;
-  if (kp >= it.k_end) return;
-  const int id = __ldg(a.kv_indices + it.loc.idx_base + kp);
-  if (id < 0 || (a.pool_rows > 0 && id >= a.pool_rows)) return;
-  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(a.kv_pool + (size_t)id * kRow), "r"(kRow * 2)
-               : "memory");
+// Waits until ring tile t is loaded (every lane acquires it).
+__device__ __forceinline__ bool wait_ring(const VerifyArgs& a, Ctrl* c, int t) {
+  return wait_cta(&c->ifull[t % NIDX], (t / NIDX) & 1, c, a.status);
+}
+__device__ __forceinline__ void release_ring(Ctrl* c, int t, int lane) {
+  __syncwarp();
+  if (lane == 0) mbar_arrive(&c->iempty[t % NIDX]);
 }
 
-__device__ __forceinline__ int scorer_producer_rank(int warp) {
-  if (warp == 0) return 0;
-  if (warp == 2) return 1;
-  if (warp == 3) return 2;
-  if (warp >= 8) return warp - 5;
-  return -1;
+// cp.async of one 64-column chunk (columns 64*col_chunk ..) of the key rows
+// ids[j] (chunk rows row0 + 4 j + lane/8, j < N) into `dst` (row k at
+// dst + 128 k, 128-byte swizzled); a missing key (-1) writes zeros.
+template <int N>
+__device__ __forceinline__ void lsu_chunk(const uint16_t* pool, uint8_t* dst, int col_chunk, int row0,
+                                          const int (&ids)[N], int lane) {
+  const int piece = lane & 7;
+  const uint32_t base = smem_u32(dst);
+#pragma unroll
+  for (int j = 0; j < N; ++j) {
+    const int row = row0 + 4 * j + (lane >> 3);
+    const int id = ids[j];
+    const uint16_t* src = pool + (size_t)(id < 0 ? 0 : id) * kRow + col_chunk * 64 + piece * 8;
+    cp_async16_zfill(base + row * 128 + ((piece ^ (row & 7)) << 4), src, id < 0 ? 0u : 16u);
+  }
 }
-__device__ __forceinline__ int acc_producer_rank(int warp) {
-  if (warp == 0) return 0;
-  if (warp == 3) return 1;
-  if (warp >= 8) return warp - 6;
-  return -1;
+// TMA gather4 of groups g = g0 .. g0+ng-1 (four keys each: keys[4g .. 4g+3])
+// of one 64-column chunk into `dst` (row k at dst + 128 k, 128-byte
+// swizzled).  A missing key reads row 0: its score is masked and its weight
+// is zero.
+__device__ __forceinline__ void tma_gather(const PoolMaps& maps, uint8_t* dst, int col_chunk, const int* keys,
+                                           int g0, int ng, uint64_t* bar) {
+  for (int g = g0; g < g0 + ng; ++g) {
+    const int4 r = *reinterpret_cast<const int4*>(keys + 4 * g);
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3, %4, %5, %6}], [%7];" ::"r"(smem_u32(dst + 4 * g * 128)),
+        "l"(&maps.row), "r"(col_chunk * 64), "r"(max(r.x, 0)), "r"(max(r.y, 0)), "r"(max(r.z, 0)),
+        "r"(max(r.w, 0)), "r"(smem_u32(bar))
+        : "memory");
+  }
+}
+// One 2-D TMA tile (a contiguous run of rows) of one 64-column chunk.
+__device__ __forceinline__ void tma_run(const CUtensorMap* map, uint8_t* dst, int col_chunk, int first_row,
+                                        uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];"
+      ::"r"(smem_u32(dst)), "l"(map), "r"(col_chunk * 64), "r"(first_row), "r"(smem_u32(bar))
+      : "memory");
+}
+
+// A TMA producer warp.  Lane 0 issues each tile's loads (`issue(t, bar)`
+// arms `bar` with the bytes and starts them) once the slot is free; lane 1
+// waits for each issued tile's bytes on the warp's own barrier and then
+// counts the warp in on the slot's full barrier.  After an expired wait lane
+// 1 still waits (fixed bound) for every tile lane 0 issued, so no load is in
+// flight when the CTA leaves.
+template <typename Issue>
+__device__ __forceinline__ void tma_producer(const VerifyArgs& a, const Item& it, Ctrl* c, int w, int lane,
+                                             Issue&& issue) {
+  volatile uint32_t* issued = &c->tma_issued[w];
+  if (lane == 0) {
+    for (int t = 0; t < it.ntiles; ++t) {
+      const int s = t & 1;
+      if (!wait_ring(a, c, t)) break;
+      const bool free = wait_clu(&c->empty[s], ((t >> 1) & 1) ^ 1, c, a.status);
+      if (free) issue(t, &c->tma[w][s]);
+      mbar_arrive(&c->iempty[t % NIDX]);
+      if (!free) break;
+      __threadfence_block();
+      *issued = (uint32_t)(t + 1);
+    }
+    __threadfence_block();
+    *issued = *issued | 0x80000000u;  // done issuing
+  } else if (lane == 1) {
+    for (int t = 0; t < it.ntiles; ++t) {
+      // Wait (bounded) until lane 0 issued tile t or stopped.
+      uint32_t v = *issued;
+      const uint64_t deadline = global_timer_ns() + kDrainNs;
+      while ((v & 0x7fffffffu) <= (uint32_t)t && !(v & 0x80000000u) && global_timer_ns() < deadline) {
+        __nanosleep(32);
+        v = *issued;
+      }
+      if ((v & 0x7fffffffu) <= (uint32_t)t) break;  // never issued
+      const uint64_t* bar = &c->tma[w][t & 1];
+      if (!mbar_wait(const_cast<uint64_t*>(bar), (t >> 1) & 1, global_timer_ns() + kDrainNs)) {
+        atomicOr(a.status, DDTREE_ST_TIMEOUT);
+        c->abort = 1;
+        break;
+      }
+      mbar_arrive(&c->full[t & 1]);
+    }
+  }
 }
 
 // ------------------------------------------------------------------ scorer
@@ -350,97 +386,106 @@ __device__ void scorer(const VerifyArgs& a, const PoolMaps& maps, const Item& it
   const uint32_t tmem = c->tmem_base;  // [0,256): Q latent; [256,384), [384,512): S
   const bool leader = (rank & 1) == 0;
   const int half = rank & 1;           // which 64 keys of each tile this CTA gathers
-  const int prank = scorer_producer_rank(warp);
 
-  if (prank >= 0) {
-    // ---- producers: this CTA's 64 keys, columns 0..575, of every tile
-    int n = 0;
-    RawIdx raw_next = raw_tile_indices(a, it, 0, lane);
+  // Producer warps: load/store unit {0, 2, 3, 12} (chunks 0..5), TMA {13, 14} (chunks 6..8).
+  const int lsu = warp == 0 ? 0 : warp == 2 ? 1 : warp == 3 ? 2 : warp == 12 ? 3 : -1;
+  const int tma = warp == 13 ? 0 : warp == 14 ? 1 : -1;
+  if (warp == kLoaderWarp) {
+    index_loader(a, it, sm, c, false);
+  } else if (lsu >= 0) {
+    constexpr int G = 16 / kLsuWarps;  // groups of four keys per warp (of the half's 16)
     for (int t = 0; t < it.ntiles; ++t) {
-      const TileIdx ti = finish_tile_indices(a, raw_next, lane);
-      if (t + 1 < it.ntiles) raw_next = raw_tile_indices(a, it, t + 1, lane);
-      const MyKeys mk = my_keys(ti, lane, prank, kScorerProducers, 16 * half, 16);
-      for (int u = 0; u < 9 / QU; ++u, ++n) {
-        const int slot = n % QUNITS;
-        bool ok = true;
-        if (lane == 0) ok = wait_clu(&c->kempty[slot], ((n / QUNITS) & 1) ^ 1, c, a.status);
-        if (!__shfl_sync(0xffffffffu, ok, 0)) {
-          asm volatile("cp.async.wait_all;" ::: "memory");
-          return;
-        }
+      const int s = t & 1;
+      if (!wait_ring(a, c, t)) break;
+      const int* keys = ring_tile(sm, t) + HALF * half;
+      const bool contig = c->icontig[t % NIDX] != 0;
+      int ids[G];
+#pragma unroll
+      for (int j = 0; j < G; ++j) ids[j] = keys[4 * (G * lsu + j) + (lane >> 3)];
+      release_ring(c, t, lane);
+      bool ok = true;
+      if (lane == 0) ok = wait_clu(&c->empty[s], ((t >> 1) & 1) ^ 1, c, a.status);
+      if (!__shfl_sync(0xffffffffu, ok, 0)) break;
+      uint8_t* slot = sm + Q_RING + s * KSLOT;
+      if (!contig) {  // a contiguous tile comes whole by TMA
 #pragma unroll 1
-        for (int cc = 0; cc < QU; ++cc)
-          fill_chunk(maps, a.kv_pool, sm + Q_RING + slot * QUNIT_BYTES + cc * SCHUNK, QU * u + cc, HALF * half, HALF,
-                     ti, mk, prank, lane, &c->kfull[slot], QU * u + cc >= kScorerLsuChunks);
-        cp_async_mbar_arrive(&c->kfull[slot]);
+        for (int ch = 0; ch < kScorerLsuChunks; ++ch)
+          lsu_chunk<G>(a.kv_pool, slot + ch * SCHUNK, ch, 4 * G * lsu, ids, lane);
       }
+      cp_async_mbar_arrive(&c->full[s]);
     }
     asm volatile("cp.async.wait_all;" ::: "memory");
+  } else if (tma >= 0) {
+    constexpr int G = 16 / kTmaWarps;
+    tma_producer(a, it, c, tma, lane, [&](int t, uint64_t* bar) {
+      const int s = t & 1;
+      const int* keys = ring_tile(sm, t) + HALF * half;
+      uint8_t* slot = sm + Q_RING + s * KSLOT;
+      if (c->icontig[t % NIDX]) {
+        mbar_arrive_expect_tx(bar, tma == 0 ? KSLOT : 0);
+        if (tma == 0)
+          for (int ch = 0; ch < 9; ++ch)
+            tma_run(&maps.half, slot + ch * SCHUNK, ch, c->ifirst[t % NIDX] + HALF * half, bar);
+      } else {
+        mbar_arrive_expect_tx(bar, (9 - kScorerLsuChunks) * G * 512);
+        for (int ch = kScorerLsuChunks; ch < 9; ++ch) tma_gather(maps, slot + ch * SCHUNK, ch, keys, G * tma, G, bar);
+      }
+    });
   } else if (warp == 1 && lane == 0) {
     if (leader) {
-      // ---- MMA issuer for the pair
+      // ---- MMA issuer for the pair: one tile at a time, once all of it landed
       constexpr uint32_t idesc = idesc_bf16_f32(256, 128, false, false);
       const uint64_t rope_desc = desc_sw128(smem_u32(sm + Q_ROPE), 16, 1024);
-      int n = 0;
       bool ok = wait_clu(&c->q_ready, 0, c, a.status);
       tc_fence_after();
       for (int t = 0; t < it.ntiles && ok; ++t) {
         const int s = t & 1;
+        const uint32_t ph = (t >> 1) & 1;
         const uint32_t sbuf = tmem + 256 + 128 * s;
-        if (!wait_clu(&c->sempty[s], ((t >> 1) & 1) ^ 1, c, a.status)) { ok = false; break; }
+        if (!wait_clu(&c->sempty[s], ph ^ 1, c, a.status) || !wait_cta(&c->full[s], ph, c, a.status) ||
+            !wait_clu(&c->peer[s], ph, c, a.status))
+          break;
+        fence_async_smem();  // cp.async (generic proxy) data -> tensor-core reads
         tc_fence_after();
-        for (int u = 0; u < 9 / QU; ++u, ++n) {
-          const int slot = n % QUNITS;
-          const uint32_t ph = (n / QUNITS) & 1;
-          if (!wait_clu(&c->kfull[slot], ph, c, a.status) || !wait_clu(&c->kpeer[slot], ph, c, a.status)) {
-            ok = false;
-            break;
-          }
-          fence_async_smem();  // cp.async (generic proxy) data -> tensor-core reads
-          tc_fence_after();
+        const uint8_t* slot = sm + Q_RING + s * KSLOT;
 #pragma unroll
-          for (int cc = 0; cc < QU; ++cc) {  // chunk ch: K steps 4ch .. 4ch+3 of the 36
-            const int ch = QU * u + cc;
-            const uint64_t kdesc = desc_sw128(smem_u32(sm + Q_RING + slot * QUNIT_BYTES + cc * SCHUNK), 16, 1024);
-            if (ch < 8) mma2_ts_x4(sbuf, tmem + ch * 32, kdesc, idesc, ch > 0);  // latent: Q from TMEM
-            else mma2_ss_x4<2, 2>(sbuf, rope_desc, kdesc, idesc, 1);            // rope: Q from shared memory
-          }
-          commit2(&c->kempty[slot], kScorerPair);
+        for (int ch = 0; ch < 9; ++ch) {  // chunk ch: K steps 4ch .. 4ch+3 of the 36
+          const uint64_t kdesc = desc_sw128(smem_u32(slot + ch * SCHUNK), 16, 1024);
+          if (ch < 8) mma2_ts_x4(sbuf, tmem + ch * 32, kdesc, idesc, ch > 0);  // latent: Q from TMEM
+          else mma2_ss_x4<2, 2>(sbuf, rope_desc, kdesc, idesc, 1);            // rope: Q from shared memory
         }
-        if (ok) commit2(&c->sfull[s], kScorerPair);
+        commit2(&c->empty[s], kScorerPair);
+        commit2(&c->sfull[s], kScorerPair);
       }
       commit2(&c->mma_done, kScorerPair);
     } else {
-      // ---- follower: forward "my half of unit n landed" to the leader
-      const uint32_t lead_kpeer = map_cluster(smem_u32(&c->kpeer[0]), rank - 1);
+      // ---- follower: forward "my slot of tile t is full" to the leader
+      const uint32_t lead_peer = map_cluster(smem_u32(&c->peer[0]), rank - 1);
       // The leader's MMAs read this CTA's Q too: it must be in place before
       // the first forward.
       if (!wait_clu(&c->q_ready, 0, c, a.status)) return;
-      int n = 0;
       for (int t = 0; t < it.ntiles; ++t) {
-        for (int u = 0; u < 9 / QU; ++u, ++n) {
-          const int slot = n % QUNITS;
-          if (!wait_clu(&c->kfull[slot], (n / QUNITS) & 1, c, a.status)) return;
-          fence_async_smem();
-          remote_arrive(lead_kpeer + slot * 8);
-        }
+        const int s = t & 1;
+        if (!wait_cta(&c->full[s], (t >> 1) & 1, c, a.status)) return;
+        fence_async_smem();
+        signal_remote(lead_peer + s * 8);
       }
     }
-  } else if (warp >= 4 && warp < 8) {
-    // ---- softmax: thread = query row r of this CTA's tile
-    const int r = tid - 128;
-    const int w = warp - 4;
+  } else if (warp >= 4 && warp < 12) {
+    // ---- softmax: two warpgroups; thread = (query row r, key half hw)
+    const int hw = warp >= 8 ? 1 : 0;
+    const int w = warp & 3;
+    const int r = 32 * w + lane;
     const int req_row = it.row0 + r;
     const bool row_ok = req_row < a.rows_per_req;
+    const uint32_t lane_addr = tmem + ((uint32_t)(w * 32) << 16);
     {
-      // First, this row of Q into place while the producers already gather
-      // keys: latent -> TMEM lane r as packed bf16 pairs, rope -> shared
-      // memory (K-major, 128-byte swizzle).  16 loads in flight per thread.
+      // Q into place while the producers already gather: this half's 256
+      // latent values -> TMEM lane r, this half's 32 rope values -> smem.
       const size_t g = (size_t)it.loc.b * a.rows_per_req + (row_ok ? req_row : 0);
-      const uint4* ql = reinterpret_cast<const uint4*>(a.q_latent + g * a.q_lat_stride);
-      const uint32_t lane_addr = tmem + ((uint32_t)(w * 32) << 16);
+      const uint4* ql = reinterpret_cast<const uint4*>(a.q_latent + g * a.q_lat_stride) + 32 * hw;
 #pragma unroll 1
-      for (int b4 = 0; b4 < 4; ++b4) {
+      for (int b4 = 0; b4 < 2; ++b4) {
         uint4 x[16];
 #pragma unroll
         for (int e = 0; e < 16; ++e) x[e] = row_ok ? __ldg(ql + 16 * b4 + e) : make_uint4(0, 0, 0, 0);
@@ -452,16 +497,16 @@ __device__ void scorer(const VerifyArgs& a, const PoolMaps& maps, const Item& it
             v[4 * e] = x[4 * q + e].x; v[4 * e + 1] = x[4 * q + e].y;
             v[4 * e + 2] = x[4 * q + e].z; v[4 * e + 3] = x[4 * q + e].w;
           }
-          tmem_st16(lane_addr + 64 * b4 + 16 * q, v);
+          tmem_st16(lane_addr + 128 * hw + 64 * b4 + 16 * q, v);
         }
       }
-      const uint4* qr = reinterpret_cast<const uint4*>(a.q_rope + g * a.q_rope_stride);
-      uint4 y[8];
+      const uint4* qr = reinterpret_cast<const uint4*>(a.q_rope + g * a.q_rope_stride) + 4 * hw;
+      uint4 y[4];
 #pragma unroll
-      for (int c16 = 0; c16 < 8; ++c16) y[c16] = row_ok ? __ldg(qr + c16) : make_uint4(0, 0, 0, 0);
+      for (int c16 = 0; c16 < 4; ++c16) y[c16] = row_ok ? __ldg(qr + c16) : make_uint4(0, 0, 0, 0);
 #pragma unroll
-      for (int c16 = 0; c16 < 8; ++c16)
-        *reinterpret_cast<uint4*>(sm + Q_ROPE + r * 128 + ((c16 ^ (r & 7)) << 4)) = y[c16];
+      for (int c16 = 0; c16 < 4; ++c16)
+        *reinterpret_cast<uint4*>(sm + Q_ROPE + r * 128 + (((4 * hw + c16) ^ (r & 7)) << 4)) = y[c16];
       tmem_st_wait();
       fence_async_smem();
       tc_fence_before();
@@ -471,50 +516,32 @@ __device__ void scorer(const VerifyArgs& a, const PoolMaps& maps, const Item& it
     const uint64_t anc = row_ok ? c->anc[req_row / a.n_heads] : 0ull;
     const float scale2 = a.sm_scale * 1.4426950408889634f;  // scores in log2 units
     float m_ref = -INFINITY, l = 0.f;
-    const uint32_t my_lane_addr = (uint32_t)(w * 32) << 16;
     const uint32_t acc_rank = rank + 2;
     const uint32_t peer_pbuf = map_cluster(smem_u32(sm + V_PBUF), acc_rank);
     const uint32_t peer_pfull = map_cluster(smem_u32(&c->pfull[0]), acc_rank);
     const uint32_t lead_sempty = map_cluster(smem_u32(&c->sempty[0]), rank & ~1u);
-    // Index of this lane's key in the next tile (warp w covers keys
-    // 32w .. 32w+31), loaded one tile ahead so the load is off the loop's path.
-    auto tile_has_key = [&](int tile) { return tile < it.ntiles && it.k_begin + tile * TK + 32 * w + lane < it.k_end; };
-    auto tile_key_index = [&](int tile) {
-      return tile_has_key(tile) ? __ldg(a.kv_indices + it.loc.idx_base + it.k_begin + tile * TK + 32 * w + lane) : -1;
-    };
-    int id_next = tile_key_index(0);
     for (int t = 0; t < it.ntiles; ++t) {
       const int s = t & 1;
-      const int k0 = it.k_begin + t * TK;
-      {  // valid-key bits of this tile
-        const int id = id_next;
-        id_next = tile_key_index(t + 1);
-        bool v = false;
-        if (tile_has_key(t)) {
-          v = id >= 0 && (a.pool_rows <= 0 || id < a.pool_rows);
-          if (!v) atomicOr(a.status, DDTREE_ST_BAD_INDEX);
-        }
-        const uint32_t bits = __ballot_sync(0xffffffffu, v);
-        if (lane == 0) c->key_mask[s][w] = bits;
+      const int k0 = it.k_begin + t * TK + 64 * hw;  // first key of this half
+      // Valid-key bits of this half (lane j: keys j and 32 + j).
+      uint32_t km[2] = {0u, 0u};
+      if (wait_ring(a, c, t)) {
+        const int* keys = ring_tile(sm, t) + 64 * hw;
+#pragma unroll
+        for (int q = 0; q < 2; ++q) km[q] = __ballot_sync(0xffffffffu, keys[32 * q + lane] >= 0);
+        release_ring(c, t, lane);
       }
       wait_clu(&c->sfull[s], (t >> 1) & 1, c, a.status);  // on expiry: continue, stop below
       tc_fence_after();
-      uint32_t xr[4][32];  // raw fp32 scores of this row, 128 keys
+      uint32_t xr[2][32];  // raw fp32 scores of this row, this half's 64 keys
 #pragma unroll
-      for (int q = 0; q < 4; ++q) tmem_ld32(tmem + my_lane_addr + 256 + 128 * s + 32 * q, xr[q]);
+      for (int q = 0; q < 2; ++q) tmem_ld32(lane_addr + 256 + 128 * s + 64 * hw + 32 * q, xr[q]);
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) remote_arrive(lead_sempty + s * 8);  // S buffer s read (leader counts 8 warps)
-      named_bar(1, 128);
-      uint32_t km[4];
+      if (lane == 0) signal_remote(lead_sempty + s * 8);  // S buffer s read (leader counts 16 warps)
+      uint32_t mw[2];
 #pragma unroll
-      for (int q = 0; q < 4; ++q) km[q] = c->key_mask[s][q];
-      // Visible keys of this row as 4 x 32 bits: a valid index, and for a
-      // tree key (position P + j) node j must be an ancestor of the row's
-      // node (or the node itself).  One select per score applies the mask.
-      uint32_t mw[4];
-#pragma unroll
-      for (int q = 0; q < 4; ++q) {
+      for (int q = 0; q < 2; ++q) {
         uint32_t bits = row_ok ? km[q] : 0u;
         const int lo = k0 + 32 * q - it.loc.P;  // tree index of key 32q (negative: prefix)
         if (lo > -32) {
@@ -526,26 +553,33 @@ __device__ void scorer(const VerifyArgs& a, const PoolMaps& maps, const Item& it
         mw[q] = bits;
       }
       float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+      if ((mw[0] & mw[1]) == 0xffffffffu) {  // all visible: no selects
 #pragma unroll
-      for (int k = 0; k < TK; ++k) {
-        const float v = ((mw[k >> 5] >> (k & 31)) & 1u) ? __uint_as_float(xr[k >> 5][k & 31]) : -INFINITY;
-        xr[k >> 5][k & 31] = __float_as_uint(v);
-        mx[k & 3] = fmaxf(mx[k & 3], v);
+        for (int k = 0; k < 64; ++k) mx[k & 3] = fmaxf(mx[k & 3], __uint_as_float(xr[k >> 5][k & 31]));
+      } else {
+#pragma unroll
+        for (int k = 0; k < 64; ++k) {
+          const float v = ((mw[k >> 5] >> (k & 31)) & 1u) ? __uint_as_float(xr[k >> 5][k & 31]) : -INFINITY;
+          xr[k >> 5][k & 31] = __float_as_uint(v);
+          mx[k & 3] = fmaxf(mx[k & 3], v);
+        }
       }
-      const float mt = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])) * scale2;
+      const float mh = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])) * scale2;
+      c->xmax[hw][r] = mh;
+      // The staging buffer is free once the previous tile's copy has read it.
+      if (r == 0 && hw == 0) asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+      named_bar(1, 256);
+      const float mt = fmaxf(mh, c->xmax[hw ^ 1][r]);
       float alpha = 1.f;
       if (mt > m_ref + kLazyRescale) {  // also true on the first finite max
         alpha = (m_ref == -INFINITY) ? 0.f : ex2_approx(m_ref - mt);
         m_ref = mt;
       }
       const float nm = (m_ref == -INFINITY) ? 0.f : -m_ref;
-      // The staging buffer is free once the previous tile's copy has read it.
-      if (r == 0) asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
-      named_bar(1, 128);
       uint8_t* stg = sm + Q_STAGE;
       float ps[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-      for (int cc = 0; cc < 16; ++cc) {  // 16-byte chunk cc = keys 8cc .. 8cc+7
+      for (int cc = 0; cc < 8; ++cc) {  // 16-byte chunk cc = keys 8cc .. 8cc+7 of this half
         uint32_t pk[4];
 #pragma unroll
         for (int h = 0; h < 4; ++h) {
@@ -556,20 +590,21 @@ __device__ void scorer(const VerifyArgs& a, const PoolMaps& maps, const Item& it
           __nv_bfloat162 b = __floats2bfloat162_rn(p0, p1);
           pk[h] = *reinterpret_cast<uint32_t*>(&b);
         }
-        const int atom = cc >> 3, c16 = cc & 7;
-        *reinterpret_cast<uint4*>(stg + atom * VCHUNK + r * 128 + ((c16 ^ (r & 7)) << 4)) =
+        *reinterpret_cast<uint4*>(stg + hw * VCHUNK + r * 128 + ((cc ^ (r & 7)) << 4)) =
             make_uint4(pk[0], pk[1], pk[2], pk[3]);
       }
       const float sum = (row_ok ? 1.f : 0.f) * ((ps[0] + ps[1]) + (ps[2] + ps[3]));
       l = l * alpha + sum;
       float* meta = reinterpret_cast<float*>(stg + PTILE);
-      meta[r] = alpha;
-      meta[128 + r] = l;
-      const uint32_t flag = __ballot_sync(0xffffffffu, t > 0 && alpha != 1.f);
-      if (lane == 0) reinterpret_cast<uint32_t*>(meta + 256)[w] = flag;
+      meta[128 * (1 + hw) + r] = l;
+      if (hw == 0) {
+        meta[r] = alpha;
+        const uint32_t flag = __ballot_sync(0xffffffffu, t > 0 && alpha != 1.f);
+        if (lane == 0) reinterpret_cast<uint32_t*>(meta + 384)[w] = flag;
+      }
       fence_async_smem();
-      named_bar(1, 128);
-      if (r == 0 && !aborted(c)) {
+      named_bar(1, 256);
+      if (r == 0 && hw == 0 && !aborted(c)) {
         // The accumulator's P buffer s is free once it finished tile t-2.
         if (wait_clu(&c->pfree[s], ((t >> 1) & 1) ^ 1, c, a.status)) {
           asm volatile(
@@ -579,13 +614,16 @@ __device__ void scorer(const VerifyArgs& a, const PoolMaps& maps, const Item& it
               : "memory");
         }
       }
-      if (named_bar_or(1, 128, aborted(c))) break;
+      if (named_bar_or(1, 256, aborted(c))) break;
     }
-    if (row_ok) {
+    if (hw == 1) c->xmax[1][r] = l;
+    named_bar(1, 256);
+    if (hw == 0 && row_ok) {
+      const float lt = l + c->xmax[1][r];
       a.partial_lse[(size_t)it.slot * a.rows_per_req + req_row] =
-          (l > 0.f) ? (m_ref + log2f(l)) * 0.6931471805599453f : -INFINITY;
+          (lt > 0.f) ? (m_ref + log2f(lt)) * 0.6931471805599453f : -INFINITY;
     }
-    if (r == 0) asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+    if (r == 0 && hw == 0) asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
   }
 }
 
@@ -597,86 +635,88 @@ __device__ void accumulator(const VerifyArgs& a, const PoolMaps& maps, const Ite
   const bool leader = (rank & 1) == 0;
   const int par = rank & 1;            // value chunks 2q + par of every tile
   const uint32_t scorer_rank = rank - 2;
-  const int prank = acc_producer_rank(warp);
+  // Producer warps: load/store unit {0, 3, 8, 9} (q = 0..2), TMA {10, 11} (q = 3).
+  const int lsu = warp == 0 ? 0 : warp == 3 ? 1 : warp == 8 ? 2 : warp == 9 ? 3 : -1;
+  const int tma = warp == 10 ? 0 : warp == 11 ? 1 : -1;
 
-  if (prank >= 0) {
-    // ---- producers: value chunks 2q+par (q = 0..3), all 128 keys
-    int n = 0;
-    RawIdx raw_next = raw_tile_indices(a, it, 0, lane);
+  if (warp == kLoaderWarp) {
+    index_loader(a, it, sm, c, true);
+  } else if (lsu >= 0) {
+    constexpr int G = 32 / kLsuWarps;  // groups of four keys per warp (of the tile's 32)
     for (int t = 0; t < it.ntiles; ++t) {
-      const TileIdx ti = finish_tile_indices(a, raw_next, lane);
-      if (t + 1 < it.ntiles) raw_next = raw_tile_indices(a, it, t + 1, lane);
-      const MyKeys mk = my_keys(ti, lane, prank, kAccProducers, 0, 32);
-      for (int u = 0; u < 4 / VU; ++u, ++n) {
-        const int slot = n % VUNITS;
-        bool ok = true;
-        if (lane == 0) ok = wait_clu(&c->vempty[slot], ((n / VUNITS) & 1) ^ 1, c, a.status);
-        if (!__shfl_sync(0xffffffffu, ok, 0)) {
-          asm volatile("cp.async.wait_all;" ::: "memory");
-          return;
-        }
+      const int s = t & 1;
+      if (!wait_ring(a, c, t)) break;
+      const int* keys = ring_tile(sm, t);
+      const bool contig = c->icontig[t % NIDX] != 0;
+      int ids[G];
+#pragma unroll
+      for (int j = 0; j < G; ++j) ids[j] = keys[4 * (G * lsu + j) + (lane >> 3)];
+      release_ring(c, t, lane);
+      bool ok = true;
+      if (lane == 0) ok = wait_clu(&c->empty[s], ((t >> 1) & 1) ^ 1, c, a.status);
+      if (!__shfl_sync(0xffffffffu, ok, 0)) break;
+      uint8_t* slot = sm + V_RING + s * VSLOT;
+      if (!contig) {
 #pragma unroll 1
-        for (int cc = 0; cc < VU; ++cc)
-          fill_chunk(maps, a.kv_pool, sm + V_RING + slot * VUNIT_BYTES + cc * VCHUNK, 2 * (VU * u + cc) + par, 0, TK,
-                     ti, mk, prank, lane, &c->vfull[slot], VU * u + cc >= kAccLsuChunks);
-        cp_async_mbar_arrive(&c->vfull[slot]);
+        for (int q = 0; q < kAccLsuChunks; ++q) lsu_chunk<G>(a.kv_pool, slot + q * VCHUNK, 2 * q + par, 4 * G * lsu, ids, lane);
       }
+      cp_async_mbar_arrive(&c->full[s]);
     }
     asm volatile("cp.async.wait_all;" ::: "memory");
+  } else if (tma >= 0) {
+    constexpr int G = 32 / kTmaWarps;
+    tma_producer(a, it, c, tma, lane, [&](int t, uint64_t* bar) {
+      const int s = t & 1;
+      const int* keys = ring_tile(sm, t);
+      uint8_t* slot = sm + V_RING + s * VSLOT;
+      if (c->icontig[t % NIDX]) {
+        mbar_arrive_expect_tx(bar, tma == 0 ? VSLOT : 0);
+        if (tma == 0)
+          for (int q = 0; q < 4; ++q) tma_run(&maps.tile, slot + q * VCHUNK, 2 * q + par, c->ifirst[t % NIDX], bar);
+      } else {
+        mbar_arrive_expect_tx(bar, (4 - kAccLsuChunks) * G * 512);
+        for (int q = kAccLsuChunks; q < 4; ++q) tma_gather(maps, slot + q * VCHUNK, 2 * q + par, keys, G * tma, G, bar);
+      }
+    });
   } else if (warp == 1 && lane == 0) {
     if (leader) {
       // ---- MMA issuer for the pair: O[rows, 128q .. 128q+127] += P V
       constexpr uint32_t idesc = idesc_bf16_f32(256, 128, false, true);  // A = P K-major, B = V MN-major
-      int n = 0;
-      bool ok = true;
-      for (int t = 0; t < it.ntiles && ok; ++t) {
+      for (int t = 0; t < it.ntiles; ++t) {
         const int s = t & 1;
         const uint32_t ph = (t >> 1) & 1;
         if (!wait_clu(&c->pfull[s], ph, c, a.status) || !wait_clu(&c->ppeer[s], ph, c, a.status) ||
-            !wait_clu(&c->corr_done[s], ph, c, a.status)) {
-          ok = false;
+            !wait_clu(&c->corr_done[s], ph, c, a.status) || !wait_cta(&c->full[s], ph, c, a.status) ||
+            !wait_clu(&c->peer[s], ph, c, a.status))
           break;
-        }
+        fence_async_smem();  // cp.async (generic proxy) data -> tensor-core reads
         tc_fence_after();
         const uint64_t pdesc = desc_sw128(smem_u32(sm + V_PBUF + s * PBUF), 16, 1024);
-        for (int u = 0; u < 4 / VU; ++u, ++n) {
-          const int slot = n % VUNITS;
-          const uint32_t vph = (n / VUNITS) & 1;
-          if (!wait_clu(&c->vfull[slot], vph, c, a.status) || !wait_clu(&c->vpeer[slot], vph, c, a.status)) {
-            ok = false;
-            break;
-          }
-          fence_async_smem();  // cp.async (generic proxy) data -> tensor-core reads
-          tc_fence_after();
+        const uint8_t* slot = sm + V_RING + s * VSLOT;
 #pragma unroll
-          for (int cc = 0; cc < VU; ++cc) {
-            const int q = VU * u + cc;
-            const uint64_t vdesc = desc_sw128(smem_u32(sm + V_RING + slot * VUNIT_BYTES + cc * VCHUNK), VCHUNK, 1024);
-            // K steps 0..3 read P atom 0 (keys 0..63), 4..7 atom 1; V advances
-            // 16 keys (2 KB) per step.
-            mma2_ss_x4<2, 128>(tmem + 128 * q, pdesc, vdesc, idesc, t > 0 ? 1u : 0u);
-            mma2_ss_x4<2, 128>(tmem + 128 * q, pdesc + (VCHUNK >> 4), vdesc + 512, idesc, 1u);
-          }
-          commit2(&c->vempty[slot], kAccPair);
+        for (int q = 0; q < 4; ++q) {
+          const uint64_t vdesc = desc_sw128(smem_u32(slot + q * VCHUNK), VCHUNK, 1024);
+          // K steps 0..3 read P atom 0 (keys 0..63), 4..7 atom 1; V advances
+          // 16 keys (2 KB) per step.
+          mma2_ss_x4<2, 128>(tmem + 128 * q, pdesc, vdesc, idesc, t > 0 ? 1u : 0u);
+          mma2_ss_x4<2, 128>(tmem + 128 * q, pdesc + (VCHUNK >> 4), vdesc + 512, idesc, 1u);
         }
-        if (ok) commit2(&c->pvdone[s], kAccPair);
+        commit2(&c->empty[s], kAccPair);
+        commit2(&c->pvdone[s], kAccPair);
       }
       commit2(&c->mma_done, kAccPair);
     } else {
-      // ---- follower: forward "my P tile / my value chunk landed" to the leader
+      // ---- follower: forward "my P tile / my slot of tile t is full" to the leader
       const uint32_t lead_ppeer = map_cluster(smem_u32(&c->ppeer[0]), rank - 1);
-      const uint32_t lead_vpeer = map_cluster(smem_u32(&c->vpeer[0]), rank - 1);
-      int n = 0;
+      const uint32_t lead_peer = map_cluster(smem_u32(&c->peer[0]), rank - 1);
       for (int t = 0; t < it.ntiles; ++t) {
         const int s = t & 1;
-        if (!wait_clu(&c->pfull[s], (t >> 1) & 1, c, a.status)) return;
-        remote_arrive(lead_ppeer + s * 8);
-        for (int u = 0; u < 4 / VU; ++u, ++n) {
-          const int slot = n % VUNITS;
-          if (!wait_clu(&c->vfull[slot], (n / VUNITS) & 1, c, a.status)) return;
-          fence_async_smem();
-          remote_arrive(lead_vpeer + slot * 8);
-        }
+        const uint32_t ph = (t >> 1) & 1;
+        if (!wait_clu(&c->pfull[s], ph, c, a.status)) return;
+        signal_remote(lead_ppeer + s * 8);
+        if (!wait_cta(&c->full[s], ph, c, a.status)) return;
+        fence_async_smem();
+        signal_remote(lead_peer + s * 8);
       }
     }
   } else if (warp == 2 && lane == 0) {
@@ -687,7 +727,7 @@ __device__ void accumulator(const VerifyArgs& a, const PoolMaps& maps, const Ite
       const int s = t & 1;
       if (!wait_clu(&c->pvdone[s], (t >> 1) & 1, c, a.status)) break;
       if (t + 2 < it.ntiles) mbar_arrive_expect_tx(&c->pfull[s], PCOPY);
-      remote_arrive(sc_pfree + s * 8);
+      signal_remote(sc_pfree + s * 8);
     }
   } else if (warp >= 4 && warp < 8) {
     // ---- correction + epilogue: thread = row r (TMEM lane r)
@@ -697,15 +737,13 @@ __device__ void accumulator(const VerifyArgs& a, const PoolMaps& maps, const Ite
     const uint32_t sc_pfree = map_cluster(smem_u32(&c->pfree[0]), scorer_rank);
     const uint32_t lead_corr = map_cluster(smem_u32(&c->corr_done[0]), rank & ~1u);
     float lfin = 0.f;
-    for (int t = 0; t < kL2Ahead; ++t) prefetch_tile_l2(a, it, t, r);
     for (int t = 0; t < it.ntiles; ++t) {
       const int s = t & 1;
-      prefetch_tile_l2(a, it, t + kL2Ahead, r);
       wait_clu(&c->pfull[s], (t >> 1) & 1, c, a.status);  // on expiry: continue, stop below
       const uint8_t* pb = sm + V_PBUF + s * PBUF;
       const float* meta = reinterpret_cast<const float*>(pb + PTILE);
-      const uint32_t* flags = reinterpret_cast<const uint32_t*>(meta + 256);
-      lfin = meta[128 + r];
+      const uint32_t* flags = reinterpret_cast<const uint32_t*>(meta + 384);
+      lfin = meta[128 + r] + meta[256 + r];
       if (flags[0] | flags[1] | flags[2] | flags[3]) {
         const float alpha = meta[r];
         // O must hold PV of tiles < t before it is rescaled.
@@ -726,14 +764,14 @@ __device__ void accumulator(const VerifyArgs& a, const PoolMaps& maps, const Ite
       }
       // Every tile: this CTA's O is ready for PV(t) (the leader counts 8 warps).
       __syncwarp();
-      if (lane == 0) remote_arrive(lead_corr + s * 8);
+      if (lane == 0) signal_remote(lead_corr + s * 8);
       // Second release of P buffer s: its metadata has been read.
       const bool stop = named_bar_or(2, 128, aborted(c));
-      if (r == 0 && !stop) remote_arrive(sc_pfree + s * 8);
+      if (r == 0 && !stop) release_remote(sc_pfree + s * 8);
       if (stop) break;
     }
-    // Epilogue: O_s = O / l, written as fp32 rows of the workspace.  Each
-    // 32-column slice of the tile goes TMEM -> registers -> a swizzled
+    // Epilogue: O_s = O / l, written as bf16 rows of the workspace.  Each
+    // 64-column slice of the tile goes TMEM -> registers -> a swizzled
     // shared-memory box (4 rotating 16 KB boxes in the free value ring) ->
     // one TMA store, which writes whole rows' slices coalesced and clips
     // the rows past the request.
@@ -745,34 +783,48 @@ __device__ void accumulator(const VerifyArgs& a, const PoolMaps& maps, const Ite
       const float inv = lfin > 0.f ? 1.f / lfin : 0.f;
       const bool store = it.row0 < a.rows_per_req;
       constexpr int kBox = ROWS * 128;  // 16 KB
-      for (int q = 0; q < kLatent / 32; ++q) {
+      for (int q = 0; q < kLatent / 64; ++q) {
         uint8_t* box = sm + V_RING + (q & 3) * kBox;
         if (q >= 4) {
           // The store issued from this box four slices ago must have read it.
           if (r == 0) asm volatile("cp.async.bulk.wait_group.read 3;" ::: "memory");
           named_bar(2, 128);
         }
-        uint32_t v[32];
-        tmem_ld32(lane_addr + 32 * q, v);
 #pragma unroll
-        for (int j = 0; j < 8; ++j)
-          *reinterpret_cast<float4*>(box + r * 128 + ((j ^ (r & 7)) << 4)) =
-              make_float4(__uint_as_float(v[4 * j]) * inv, __uint_as_float(v[4 * j + 1]) * inv,
-                          __uint_as_float(v[4 * j + 2]) * inv, __uint_as_float(v[4 * j + 3]) * inv);
+        for (int h = 0; h < 2; ++h) {
+          uint32_t v[32];
+          tmem_ld32(lane_addr + 64 * q + 32 * h, v);
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {  // 16-byte piece 4h + j: columns 8 (4h + j) ..
+            uint32_t pk[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              __nv_bfloat162 b2 = __floats2bfloat162_rn(__uint_as_float(v[8 * j + 2 * e]) * inv,
+                                                        __uint_as_float(v[8 * j + 2 * e + 1]) * inv);
+              pk[e] = *reinterpret_cast<uint32_t*>(&b2);
+            }
+            *reinterpret_cast<uint4*>(box + r * 128 + (((4 * h + j) ^ (r & 7)) << 4)) =
+                make_uint4(pk[0], pk[1], pk[2], pk[3]);
+          }
+        }
         fence_async_smem();
         named_bar(2, 128);
         if (r == 0 && store) {
           asm volatile(
               "cp.async.bulk.tensor.3d.global.shared::cta.tile.bulk_group [%0, {%1, %2, %3}], [%4];\n"
-              "cp.async.bulk.commit_group;" ::"l"(&maps.po), "r"(32 * q), "r"(it.row0), "r"(it.slot),
+              "cp.async.bulk.commit_group;" ::"l"(&maps.po), "r"(64 * q), "r"(it.row0), "r"(it.slot),
               "r"(smem_u32(box))
               : "memory");
         }
       }
-      if (r == 0) asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+      if (r == 0) {
+        asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+        // The stores are read by other CTAs' ordinary loads in the fused merge.
+        asm volatile("fence.proxy.async;" ::: "memory");
+      }
     } else if (row_ok) {
       for (int d = 0; d < kLatent; ++d)
-        a.partial_o[((size_t)it.slot * a.rows_per_req + req_row) * kLatent + d] = 0.f;
+        a.partial_o[((size_t)it.slot * a.rows_per_req + req_row) * kLatent + d] = 0;
     }
   }
 }
@@ -798,29 +850,34 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(kThreads, 1)
   // All four CTAs see the same key range; an empty item skips all work but
   // still takes part in the cluster barriers and the pair's TMEM allocation.
 
+  if (rank < 2 && have && tid < a.n_nodes) c->par[tid] = __ldg(a.tree_parent + (size_t)it.loc.b * a.n_nodes + tid);
   if (tid == 0) {
-    for (int i = 0; i < QUNITS; ++i) {
-      mbar_init(&c->kfull[i], 32 * kScorerProducers);
-      mbar_init(&c->kpeer[i], 1);
-      mbar_init(&c->kempty[i], 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&c->full[i], 32 * kLsuWarps + kTmaWarps);  // every producer lane, each TMA warp once
+      mbar_init(&c->peer[i], 1);
+      mbar_init(&c->empty[i], 1);
+      for (int w = 0; w < kTmaWarps; ++w) mbar_init(&c->tma[w][i], 1);
     }
-    for (int i = 0; i < VUNITS; ++i) {
-      mbar_init(&c->vfull[i], 32 * kAccProducers);
-      mbar_init(&c->vpeer[i], 1);
-      mbar_init(&c->vempty[i], 1);
-    }
+    for (int w = 0; w < kTmaWarps; ++w) c->tma_issued[w] = 0;
     for (int i = 0; i < 2; ++i) {
       mbar_init(&c->sfull[i], 1);
-      mbar_init(&c->sempty[i], 8);
+      mbar_init(&c->sempty[i], 16);
       mbar_init(&c->pfree[i], 2);
       mbar_init(&c->pfull[i], 1);
       mbar_init(&c->ppeer[i], 1);
       mbar_init(&c->pvdone[i], 1);
       mbar_init(&c->corr_done[i], 8);
     }
+    // Index ring: the loader's 32 lanes fill a slot; it is released by every
+    // producer warp, and in the scorers also by the eight softmax warps.
+    for (int i = 0; i < NIDX; ++i) {
+      mbar_init(&c->ifull[i], 32);
+      mbar_init(&c->iempty[i], kLsuWarps + kTmaWarps + (rank < 2 ? 8 : 0));
+    }
     mbar_init(&c->mma_done, 1);
-    mbar_init(&c->q_ready, 4);
+    mbar_init(&c->q_ready, 8);
     c->abort = 0;
+    c->wait_ns = a.wait_ns;
     fence_mbar_init();
   }
   if (warp == 3) {
@@ -829,7 +886,6 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(kThreads, 1)
                  : "memory");
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
   }
-  if (rank < 2 && have && tid < a.n_nodes) c->par[tid] = __ldg(a.tree_parent + (size_t)it.loc.b * a.n_nodes + tid);
   __syncthreads();
   if (rank < 2 && have) {
     const int T = a.n_nodes;
@@ -849,13 +905,44 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(kThreads, 1)
   tc_fence_before();
   __syncthreads();
   // Tensor-core work writing this CTA's TMEM must be finished before it is freed.
-  if (warp == 3 && have && it.ntiles > 0) mbar_wait_cluster(&c->mma_done, 0, global_timer_ns() + kWaitNs);
+  if (warp == 3 && have && it.ntiles > 0) mbar_wait_cluster(&c->mma_done, 0, global_timer_ns() + kDrainNs);
   tc_fence_before();
   __syncthreads();
   cluster_sync();  // no remote copy or arrival may target a CTA that has exited
   tc_fence_after();
   if (warp == 3)
     asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(c->tmem_base), "r"(512) : "memory");
+
+  if (a.fused) {
+    // Merge the splits in this launch: every CTA of the grid is resident at
+    // once (cooperative launch), so each counts itself done and waits,
+    // bounded, for all others; then the warps of the grid share the
+    // (row, 128-column) merge units.  A timed-out wait anywhere writes zeros.
+    if (tid == 0) {
+      __threadfence();
+      atomicAdd(a.grid_done, 1u);
+      const uint64_t deadline = global_timer_ns() + a.wait_ns;
+      bool ok = true;
+      for (uint32_t spin = 0;; ++spin) {
+        uint32_t v;
+        asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(a.grid_done) : "memory");
+        if (v >= gridDim.x) break;
+        if ((spin & 63u) == 63u && global_timer_ns() > deadline) {
+          ok = false;
+          break;
+        }
+      }
+      if (!ok) atomicOr(a.status, DDTREE_ST_TIMEOUT);
+      uint32_t st;
+      asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(st) : "l"(a.status) : "memory");
+      c->merge_zero = (!ok || (st & DDTREE_ST_TIMEOUT)) ? 1u : 0u;
+    }
+    __syncthreads();
+    const bool zero = c->merge_zero != 0;
+    const int units = combine_units(a);
+    for (int u = blockIdx.x * (kThreads / 32) + warp; u < units; u += gridDim.x * (kThreads / 32))
+      combine_unit(a, u, tid & 31, zero);
+  }
 }
 
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
@@ -879,35 +966,31 @@ EncodeTiledFn encode_fn() {
 
 // Pool maps over [rows, 576] bf16 with 1152-byte rows, 128-byte swizzle:
 // `tile` has a 128-row box (a whole tile), `half` a 64-row box (one scorer
-// half).  Rows past the pool read as zeros; with an unknown pool size the
-// row extent is the int32 index range (the caller vouches for the indices).
+// half), `row` a 1-row box (gather4).  Rows past the pool read as zeros; with
+// an unknown pool size the row extent is the int32 index range (the caller
+// vouches for the indices).
 cudaError_t make_pool_maps(const VerifyArgs& a, PoolMaps* m) {
   EncodeTiledFn enc = encode_fn();
   if (!enc) return cudaErrorNotSupported;
   const cuuint64_t rows = a.pool_rows > 0 ? (cuuint64_t)a.pool_rows : (cuuint64_t)0x7fffffff;
   const cuuint64_t dims[2] = {(cuuint64_t)kRow, rows};
   const cuuint64_t strides[1] = {(cuuint64_t)kRow * 2};
-  const cuuint32_t box_half[2] = {64, (cuuint32_t)HALF}, box_tile[2] = {64, (cuuint32_t)TK}, es[2] = {1, 1};
+  const cuuint32_t box_half[2] = {64, (cuuint32_t)HALF}, box_tile[2] = {64, (cuuint32_t)TK}, box_row[2] = {64, 1};
+  const cuuint32_t es[2] = {1, 1};
   void* base = const_cast<uint16_t*>(a.kv_pool);
-  if (enc(&m->half, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, base, dims, strides, box_half, es,
-          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
-    return cudaErrorInvalidValue;
-  if (enc(&m->tile, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, base, dims, strides, box_tile, es,
-          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
-    return cudaErrorInvalidValue;
-  const cuuint32_t box_row[2] = {64, 1};
-  if (enc(&m->row, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, base, dims, strides, box_row, es,
-          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
-    return cudaErrorInvalidValue;
-  // Partial O: [total_splits][rows_per_req][512] fp32; rows past the request
+  const cuuint32_t* boxes[3] = {box_half, box_tile, box_row};
+  CUtensorMap* maps[3] = {&m->half, &m->tile, &m->row};
+  for (int i = 0; i < 3; ++i)
+    if (enc(maps[i], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, base, dims, strides, boxes[i], es,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return cudaErrorInvalidValue;
+  // Partial O: [total_splits][rows_per_req][512] bf16; rows past the request
   // fall outside dimension 1, so a store of a partial row tile is clipped.
   const cuuint64_t odims[3] = {(cuuint64_t)kLatent, (cuuint64_t)a.rows_per_req, (cuuint64_t)a.total_splits};
-  const cuuint64_t ostrides[2] = {(cuuint64_t)kLatent * 4, (cuuint64_t)a.rows_per_req * kLatent * 4};
-  const cuuint32_t obox[3] = {32, (cuuint32_t)ROWS, 1}, oes[3] = {1, 1, 1};
-  if (enc(&m->po, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, a.partial_o, odims, ostrides, obox, oes,
+  const cuuint64_t ostrides[2] = {(cuuint64_t)kLatent * 2, (cuuint64_t)a.rows_per_req * kLatent * 2};
+  const cuuint32_t obox[3] = {64, (cuuint32_t)ROWS, 1}, oes[3] = {1, 1, 1};
+  if (enc(&m->po, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, a.partial_o, odims, ostrides, obox, oes,
           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
     return cudaErrorInvalidValue;
@@ -941,8 +1024,24 @@ cudaError_t launch_partial_tc2(const VerifyArgs& a, cudaStream_t stream) {
   if (e != cudaSuccess) return e;
   const int row_pairs = (a.row_tiles + 1) / 2;
   dim3 grid(4 * row_pairs * a.total_splits);
-  partial_tc2_kernel<<<grid, kThreads, kSmemBytes, stream>>>(a, maps);
-  return cudaGetLastError();
+  if (!a.fused) {
+    partial_tc2_kernel<<<grid, kThreads, kSmemBytes, stream>>>(a, maps);
+    return cudaGetLastError();
+  }
+  // The fused merge waits on every CTA of the grid: a cooperative launch
+  // guarantees they are all resident (or fails to launch).
+  cudaLaunchConfig_t cfg;
+  memset(&cfg, 0, sizeof(cfg));
+  cfg.gridDim = grid;
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = kSmemBytes;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeCooperative;
+  attr[0].val.cooperative = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, partial_tc2_kernel, a, maps);
 }
 
 // How many 4-CTA clusters of this kernel the current device runs at
@@ -959,3 +1058,4 @@ cudaError_t cluster_capacity_tc2(int* clusters) {
 }
 
 }  // namespace ddtree
+

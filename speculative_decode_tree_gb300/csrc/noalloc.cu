@@ -11,7 +11,7 @@
 // image instead.
 //
 // The scratch is a file-scope device array of DDTREE_NOALLOC_SCRATCH_BYTES
-// (32 MiB).  Every GPU that loads this library keeps those bytes reserved
+// (8 MiB).  Every GPU that loads this library keeps those bytes reserved
 // until the process exits.  All calls on a device share the one array and it
 // keeps whatever the previous call left there: the status word at its start
 // is cleared on the stream at the beginning of every call, and every partial
@@ -69,7 +69,7 @@ bool fit_plan_to_scratch(ddtree_plan_t* p) {
     int64_t chunk = round_up((nkeys + splits - 1) / splits, p->tile_keys);
     int64_t s = (nkeys + chunk - 1) / chunk;
     int64_t lse_bytes = round_up(s * rows * 4, 256);
-    int64_t ws = 256 + lse_bytes + round_up(s * rows * (int64_t)kLatent * 4, 256);
+    int64_t ws = 256 + lse_bytes + round_up(s * rows * (int64_t)kLatent * 2, 256);  // bf16 partial O
     if (ws <= (int64_t)kScratchBytes) {
       p->chunk_keys = (int32_t)chunk;
       p->total_splits = (int32_t)s;
@@ -129,8 +129,11 @@ extern "C" int ddtree_verify_mla_noalloc(const ddtree_bf16_t* q_latent, const dd
   a.lse = lse;
   uint8_t* ws = static_cast<uint8_t*>(scratch);
   a.status = reinterpret_cast<uint32_t*>(ws);
+  a.grid_done = reinterpret_cast<uint32_t*>(ws + 8);
   a.partial_lse = reinterpret_cast<float*>(ws + plan.off_partial_lse);
-  a.partial_o = reinterpret_cast<float*>(ws + plan.off_partial_o);
+  a.partial_o = reinterpret_cast<uint16_t*>(ws + plan.off_partial_o);
+  a.fused = plan.fused_combine;
+  a.wait_ns = 2000000000ull;
   a.pool_rows = 0;
   a.sm_scale = sm_scale;
   a.batch = 1;
@@ -153,7 +156,7 @@ extern "C" int ddtree_verify_mla_noalloc(const ddtree_bf16_t* q_latent, const dd
   cudaError_t e = (plan.kernel == DDTREE_KERNEL_TC2)  ? launch_partial_tc2(a, s)
                   : (plan.kernel == DDTREE_KERNEL_TC) ? launch_partial_tc(a, s)
                                                       : launch_partial_simt(a, s);
-  if (e == cudaSuccess) e = launch_combine(a, s);
+  if (e == cudaSuccess && !a.fused) e = launch_combine(a, s);
   if (e != cudaSuccess) {
     cudaGetLastError();
     return DDTREE_ELAUNCH;

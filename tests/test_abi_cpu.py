@@ -51,7 +51,8 @@ def test_plan_fills_the_sms_and_sizes_the_workspace(lib):
     assert p.total_splits == -(-(65536 + 32) // p.chunk_keys)
     ws = B.ddtree_verify_mla_workspace_size(p)
     assert ws == p.workspace_bytes and ws % 256 == 0
-    assert ws >= 256 + p.total_splits * 256 * (512 + 1) * 4
+    # status block, fp32 LSE per (split, row), bf16 partial O per (split, row)
+    assert ws >= 256 + p.total_splits * 256 * 4 + p.total_splits * 256 * 512 * 2
     # Deterministic.
     q = B.ddtree_verify_mla_plan_ex(1, 32, 8, [65536], 262144, 148, B.DDTREE_KERNEL_SIMT)
     assert p.as_dict() == q.as_dict()
@@ -62,6 +63,44 @@ def test_plan_batch_splits_sum_per_request(lib):
     p = B.ddtree_verify_mla_plan_ex(8, 32, 8, prefixes, 524288, 148, B.DDTREE_KERNEL_SIMT)
     assert p.total_splits == sum(-(-(P + 32) // p.chunk_keys) for P in prefixes)
     assert p.max_keys == 189440 + 32
+
+
+# The five verify workloads' shapes (batch, heads, nodes, prefixes).
+WORKLOAD_SHAPES = {
+    "tiny": (1, 8, 4, [256]),
+    "tp8_slice": (1, 8, 16, [4096]),
+    "long_scattered": (1, 8, 32, [65536]),
+    "unsharded_heads": (1, 128, 64, [32768]),
+    "mixed_batch": (8, 8, 32, [1024, 4096, 8192, 16384, 32768, 65536, 131072, 189440]),
+}
+
+
+@pytest.mark.parametrize("name", sorted(WORKLOAD_SHAPES))
+@pytest.mark.parametrize("num_sms", [144, 148, 152])
+def test_cluster_plans_fit_one_wave_after_per_request_rounding(lib, name, num_sms):
+    """A cluster kernel's work items (row groups x every request's own split
+    count) fit the clusters the SMs hold at once, with the shortest such
+    chunk: one chunk shorter would need a second wave."""
+    b, h, t, prefixes = WORKLOAD_SHAPES[name]
+    p = B.ddtree_verify_mla_plan_ex(b, t, h, prefixes, 1 << 20, num_sms)
+    if p.kernel == B.DDTREE_KERNEL_SIMT:
+        return
+    csize = 4 if p.kernel == B.DDTREE_KERNEL_TC2 else 2
+    row_groups = (p.row_tiles + 1) // 2 if p.kernel == B.DDTREE_KERNEL_TC2 else p.row_tiles
+    capacity = num_sms // csize
+
+    def items(chunk):
+        return row_groups * sum(-(-(P + t) // chunk) for P in prefixes)
+
+    assert p.total_splits == sum(-(-(P + t) // p.chunk_keys) for P in prefixes)
+    assert p.chunk_keys % p.tile_keys == 0
+    if row_groups * b <= capacity:
+        assert items(p.chunk_keys) <= capacity
+        if p.chunk_keys > p.tile_keys:
+            assert items(p.chunk_keys - p.tile_keys) > capacity
+    else:
+        assert p.chunk_keys >= max(prefixes) + t
+    assert p.fused_combine == 0  # explicit SM counts never fuse (no residency guarantee known)
 
 
 @pytest.mark.parametrize("args", [
@@ -136,6 +175,44 @@ def test_accept_workspace_size(lib):
     assert B.ddtree_accept_greedy_workspace_size(8, 64) == 256 + 4352 + 256
     for bad in [(0, 4), (1, 0), (1, 65), (1025, 4)]:
         assert B.ddtree_accept_greedy_workspace_size(*bad) == 0
+
+
+# The five verify workloads' shapes (batch, heads, nodes, prefixes).
+WORKLOAD_SHAPES = {
+    "tiny": (1, 8, 4, [256]),
+    "tp8_slice": (1, 8, 16, [4096]),
+    "long_scattered": (1, 8, 32, [65536]),
+    "unsharded_heads": (1, 128, 64, [32768]),
+    "mixed_batch": (8, 8, 32, [1024, 4096, 8192, 16384, 32768, 65536, 131072, 189440]),
+}
+
+
+@pytest.mark.parametrize("name", sorted(WORKLOAD_SHAPES))
+@pytest.mark.parametrize("num_sms", [144, 148, 152])
+def test_cluster_plans_fit_one_wave_after_per_request_rounding(lib, name, num_sms):
+    """A cluster kernel's work items (row groups x every request's own split
+    count) fit the clusters the SMs hold at once, with the shortest such
+    chunk: one chunk shorter would need a second wave."""
+    b, h, t, prefixes = WORKLOAD_SHAPES[name]
+    p = B.ddtree_verify_mla_plan_ex(b, t, h, prefixes, 1 << 20, num_sms)
+    if p.kernel == B.DDTREE_KERNEL_SIMT:
+        return
+    csize = 4 if p.kernel == B.DDTREE_KERNEL_TC2 else 2
+    row_groups = (p.row_tiles + 1) // 2 if p.kernel == B.DDTREE_KERNEL_TC2 else p.row_tiles
+    capacity = num_sms // csize
+
+    def items(chunk):
+        return row_groups * sum(-(-(P + t) // chunk) for P in prefixes)
+
+    assert p.total_splits == sum(-(-(P + t) // p.chunk_keys) for P in prefixes)
+    assert p.chunk_keys % p.tile_keys == 0
+    if row_groups * b <= capacity:
+        assert items(p.chunk_keys) <= capacity
+        if p.chunk_keys > p.tile_keys:
+            assert items(p.chunk_keys - p.tile_keys) > capacity
+    else:
+        assert p.chunk_keys >= max(prefixes) + t
+    assert p.fused_combine == 0  # explicit SM counts never fuse (no residency guarantee known)
 
 
 @pytest.mark.parametrize("args", [(0, 4, 100), (1, 0, 100), (1, 65, 100), (1, 4, 0), (1, 4, (1 << 26) + 1)])
