@@ -26,18 +26,18 @@
 // O_s = O / l; the scorer writes lse_s.
 //
 // Gathers ("Chunk 66.1": 128-bit KV loads): the work item's indices pass
-// through a shared-memory ring filled ahead by a loader warp (which, in the
-// accumulator CTAs, also pulls every key row into L2 a ring's length ahead).
-// Load/store-unit warps copy most 64-column chunks of the scattered 1152-byte
-// rows with 16-byte cp.async while TMA warps fetch the remaining chunks with
-// gather4 loads at the same time, so both paths into shared memory are busy
-// at once; a tile whose 128 indices form one contiguous run comes by 2-D TMA
-// tile loads instead.  A TMA warp's loads complete on its own barriers (one
-// lane issues, another lane waits for each tile's bytes and then counts the
-// warp in), so every load a CTA issued is known to have landed before it
-// exits, also after an expired wait.  The follower CTA of each pair forwards
-// "my tile is complete" to the leader, whose MMA thread then issues the
-// tile's MMAs back to back.
+// through a shared-memory ring filled ahead by a loader warp.  Load/store-
+// unit warps copy the scattered 1152-byte rows as 64-column chunks with
+// 16-byte cp.async (measured faster per SM than TMA gather4 for these rows);
+// a tile whose 128 indices form one contiguous run comes by 2-D TMA tile
+// loads instead.  A TMA warp's loads complete on its own barriers (one lane
+// issues, another lane waits for each unit's bytes and then counts the warp
+// in), so every load a CTA issued is known to have landed before it exits,
+// also after an expired wait.  The scorer's key ring holds seven units of
+// three chunks (2.3 tiles), enough to keep the next tile's rows in flight
+// while a tile is multiplied.  The follower CTA of each pair forwards "my
+// unit is complete" to the leader, whose MMA thread waits for a whole tile
+// and then issues its MMAs back to back.
 //
 // Every mbarrier wait is bounded; on expiry the kernel sets
 // DDTREE_ST_TIMEOUT, stops issuing work, waits (bounded) for its own
@@ -59,14 +59,15 @@ constexpr int ROWS = 128;                // query rows per CTA
 constexpr int HALF = 64;                 // keys per scorer CTA per tile
 constexpr int SCHUNK = HALF * 128;       // scorer chunk: 64 keys x 64 columns (8 KB)
 constexpr int VCHUNK = TK * 128;         // accumulator chunk: 128 keys x 64 columns (16 KB)
-// Rings of two tiles.  Scorer slot: the 9 chunks of its 64 keys (chunk c at
-// c x 8 KB; chunks 0..5 by cp.async, 6..8 by TMA).  Accumulator slot: its 4
-// value chunks of all 128 keys (chunk q = columns 64 (2q+p) .. at q x 16 KB;
-// q = 0..2 by cp.async, q = 3 by TMA).
-constexpr int KSLOT = 9 * SCHUNK;        // 72 KB
+// Scorer ring: units of three chunks of its 64 keys (tile t = units 3t ..
+// 3t+2; chunk c of a unit at c x 8 KB), seven unit slots.  Accumulator ring:
+// whole tiles of its 4 value chunks of all 128 keys (chunk q = columns
+// 64 (2q+p) .. at q x 16 KB), two slots.
+constexpr int QUNIT = 3 * SCHUNK;        // 24 KB
+constexpr int QSLOTS = 7;
 constexpr int VSLOT = 4 * VCHUNK;        // 64 KB
-constexpr int kScorerLsuChunks = 6;
-constexpr int kAccLsuChunks = 3;
+constexpr int VSLOTS = 2;
+constexpr int kMaxSlots = QSLOTS;
 constexpr int PTILE = 32768;             // bf16 P tile: 2 swizzle atoms of 128 rows x 128 B
 constexpr int META = 1552;               // alpha[128], l0[128], l1[128], flag words[4]
 constexpr int PCOPY = PTILE + META;      // bytes shipped per tile (multiple of 16)
@@ -80,28 +81,28 @@ constexpr float kLazyRescale = 8.0f;     // rescale only when the max grows by >
 // Tensor-core work must be complete before TMEM is freed: this wait keeps a
 // fixed bound whatever the caller's limit.
 constexpr uint64_t kDrainNs = 2000000000ull;
-constexpr uint16_t kScorerPair = 0x3, kAccPair = 0xC, kAllFour = 0xF;
+constexpr uint16_t kScorerPair = 0x3, kAccPair = 0xC;
 
 // Shared-memory map (offsets from a 1024-aligned base).
 constexpr int Q_ROPE = 0;                               // scorer: 16 KB
-constexpr int Q_RING = Q_ROPE + VCHUNK;                 // scorer: 2 x 72 KB
-constexpr int Q_STAGE = Q_RING + 2 * KSLOT;             // scorer: P staging
+constexpr int Q_RING = Q_ROPE + VCHUNK;                 // scorer: 7 x 24 KB
+constexpr int Q_STAGE = Q_RING + QSLOTS * QUNIT;        // scorer: P staging
 constexpr int Q_END = Q_STAGE + PBUF;
 constexpr int V_PBUF = 0;                               // accumulator: 2 x PBUF
 constexpr int V_RING = V_PBUF + 2 * PBUF;               // accumulator: 2 x 64 KB
-constexpr int V_END = V_RING + 2 * VSLOT;
+constexpr int V_END = V_RING + VSLOTS * VSLOT;
 constexpr int IDX_RING = (Q_END > V_END ? Q_END : V_END);  // both: NIDX x 128 int32
 constexpr int BIG_END = IDX_RING + NIDX * TK * 4;
 
 
 struct __align__(8) Ctrl {
-  // Ring slot barriers (per tile slot): full = this CTA's chunks of the tile
+  // Ring slot barriers (per unit slot): full = this CTA's chunks of the unit
   // landed (every producer lane + each TMA warp once), peer = (leader) the
   // follower's slot is full, empty = the pair's MMAs consumed the slot
   // (commit multicast to both CTAs of the pair); tma = each TMA warp's own
-  // loads of the tile landed.
-  uint64_t full[2], peer[2], empty[2], tma[kTmaWarps][2];
-  uint32_t tma_issued[kTmaWarps];  // tiles whose TMA loads a warp has issued
+  // loads of the unit landed.
+  uint64_t full[kMaxSlots], peer[kMaxSlots], empty[kMaxSlots], tma[kTmaWarps][kMaxSlots];
+  uint32_t tma_issued[kTmaWarps];  // units whose TMA loads a warp has issued
   // scorer
   uint64_t sfull[2], sempty[2], pfree[2];
   // accumulator
@@ -233,7 +234,6 @@ struct Item {
 struct PoolMaps {
   CUtensorMap half;   // 64 columns x 64 rows box: a scorer's half of a contiguous tile
   CUtensorMap tile;   // 64 columns x 128 rows box: an accumulator chunk of a contiguous tile
-  CUtensorMap row;    // 64 columns x 1 row box: four scattered rows per gather4 load
   CUtensorMap po;     // partial O [splits][rows_per_req][512] bf16, 64 columns x 128 rows box
 };
 
@@ -243,10 +243,10 @@ __device__ __forceinline__ int* ring_tile(uint8_t* sm, int t) {
 }
 
 // Loader warp: tile j's 128 indices (invalid ones -> -1, flagged) into ring
-// slot j % NIDX, with the tile's first index and whether it is one run; in
-// the accumulator CTAs each valid row is also pulled into L2 right away,
-// NIDX tiles ahead of the slowest consumer.
-__device__ void index_loader(const VerifyArgs& a, const Item& it, uint8_t* sm, Ctrl* c, bool prefetch) {
+// slot j % NIDX, with the tile's first index and whether it is one run.  (An
+// L2 prefetch of the rows from this warp measured slower: the prefetch
+// instructions held the loader back.)
+__device__ void index_loader(const VerifyArgs& a, const Item& it, uint8_t* sm, Ctrl* c) {
   const int lane = threadIdx.x & 31;
   for (int j = 0; j < it.ntiles; ++j) {
     const int slot = j % NIDX;
@@ -274,14 +274,6 @@ __device__ void index_loader(const VerifyArgs& a, const Item& it, uint8_t* sm, C
     }
     __syncwarp();
     mbar_arrive(&c->ifull[slot]);  // 32 arrivals: every lane's stores are released
-    if (prefetch) {
-#pragma unroll
-      for (int e = 0; e < 4; ++e)
-        if (v[e] >= 0)
-          asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(a.kv_pool + (size_t)v[e] * kRow),
-                       "r"(kRow * 2)
-                       : "memory");
-    }
   }
 }
 
@@ -310,22 +302,6 @@ __device__ __forceinline__ void lsu_chunk(const uint16_t* pool, uint8_t* dst, in
     cp_async16_zfill(base + row * 128 + ((piece ^ (row & 7)) << 4), src, id < 0 ? 0u : 16u);
   }
 }
-// TMA gather4 of groups g = g0 .. g0+ng-1 (four keys each: keys[4g .. 4g+3])
-// of one 64-column chunk into `dst` (row k at dst + 128 k, 128-byte
-// swizzled).  A missing key reads row 0: its score is masked and its weight
-// is zero.
-__device__ __forceinline__ void tma_gather(const PoolMaps& maps, uint8_t* dst, int col_chunk, const int* keys,
-                                           int g0, int ng, uint64_t* bar) {
-  for (int g = g0; g < g0 + ng; ++g) {
-    const int4 r = *reinterpret_cast<const int4*>(keys + 4 * g);
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes"
-        " [%0], [%1, {%2, %3, %4, %5, %6}], [%7];" ::"r"(smem_u32(dst + 4 * g * 128)),
-        "l"(&maps.row), "r"(col_chunk * 64), "r"(max(r.x, 0)), "r"(max(r.y, 0)), "r"(max(r.z, 0)),
-        "r"(max(r.w, 0)), "r"(smem_u32(bar))
-        : "memory");
-  }
-}
 // One 2-D TMA tile (a contiguous run of rows) of one 64-column chunk.
 __device__ __forceinline__ void tma_run(const CUtensorMap* map, uint8_t* dst, int col_chunk, int first_row,
                                         uint64_t* bar) {
@@ -335,46 +311,48 @@ __device__ __forceinline__ void tma_run(const CUtensorMap* map, uint8_t* dst, in
       : "memory");
 }
 
-// A TMA producer warp.  Lane 0 issues each tile's loads (`issue(t, bar)`
-// arms `bar` with the bytes and starts them) once the slot is free; lane 1
-// waits for each issued tile's bytes on the warp's own barrier and then
-// counts the warp in on the slot's full barrier.  After an expired wait lane
-// 1 still waits (fixed bound) for every tile lane 0 issued, so no load is in
-// flight when the CTA leaves.
+// A TMA producer warp over a ring of `nslots` unit slots, `upt` units per
+// tile.  Lane 0 issues each unit's loads once its slot is free
+// (`issue(n, t, u, slot, bar)` arms the warp's barrier `bar` with the unit's
+// bytes -- possibly none -- and starts them); lane 1 waits for each issued
+// unit's bytes and then counts the warp in on the slot's full barrier.  After
+// an expired wait lane 1 still waits (fixed bound) for every unit lane 0
+// issued, so no load is in flight when the CTA leaves.
 template <typename Issue>
 __device__ __forceinline__ void tma_producer(const VerifyArgs& a, const Item& it, Ctrl* c, int w, int lane,
-                                             Issue&& issue) {
+                                             int upt, int nslots, Issue&& issue) {
   volatile uint32_t* issued = &c->tma_issued[w];
+  const int nunits = it.ntiles * upt;
   if (lane == 0) {
-    for (int t = 0; t < it.ntiles; ++t) {
-      const int s = t & 1;
-      if (!wait_ring(a, c, t)) break;
-      const bool free = wait_clu(&c->empty[s], ((t >> 1) & 1) ^ 1, c, a.status);
-      if (free) issue(t, &c->tma[w][s]);
-      mbar_arrive(&c->iempty[t % NIDX]);
+    for (int n = 0; n < nunits; ++n) {
+      const int t = n / upt, u = n - t * upt, slot = n % nslots;
+      if (u == 0 && !wait_ring(a, c, t)) break;
+      const bool free = wait_clu(&c->empty[slot], ((n / nslots) & 1) ^ 1, c, a.status);
+      if (free) issue(n, t, u, slot, &c->tma[w][slot]);
+      if (!free || u == upt - 1) mbar_arrive(&c->iempty[t % NIDX]);
       if (!free) break;
       __threadfence_block();
-      *issued = (uint32_t)(t + 1);
+      *issued = (uint32_t)(n + 1);
     }
     __threadfence_block();
     *issued = *issued | 0x80000000u;  // done issuing
   } else if (lane == 1) {
-    for (int t = 0; t < it.ntiles; ++t) {
-      // Wait (bounded) until lane 0 issued tile t or stopped.
+    for (int n = 0; n < nunits; ++n) {
+      // Wait (bounded) until lane 0 issued unit n or stopped.
       uint32_t v = *issued;
       const uint64_t deadline = global_timer_ns() + kDrainNs;
-      while ((v & 0x7fffffffu) <= (uint32_t)t && !(v & 0x80000000u) && global_timer_ns() < deadline) {
+      while ((v & 0x7fffffffu) <= (uint32_t)n && !(v & 0x80000000u) && global_timer_ns() < deadline) {
         __nanosleep(32);
         v = *issued;
       }
-      if ((v & 0x7fffffffu) <= (uint32_t)t) break;  // never issued
-      const uint64_t* bar = &c->tma[w][t & 1];
-      if (!mbar_wait(const_cast<uint64_t*>(bar), (t >> 1) & 1, global_timer_ns() + kDrainNs)) {
+      if ((v & 0x7fffffffu) <= (uint32_t)n) break;  // never issued
+      const int slot = n % nslots;
+      if (!mbar_wait(&c->tma[w][slot], (n / nslots) & 1, global_timer_ns() + kDrainNs)) {
         atomicOr(a.status, DDTREE_ST_TIMEOUT);
         c->abort = 1;
         break;
       }
-      mbar_arrive(&c->full[t & 1]);
+      mbar_arrive(&c->full[slot]);
     }
   }
 }
@@ -387,15 +365,14 @@ __device__ void scorer(const VerifyArgs& a, const PoolMaps& maps, const Item& it
   const bool leader = (rank & 1) == 0;
   const int half = rank & 1;           // which 64 keys of each tile this CTA gathers
 
-  // Producer warps: load/store unit {0, 2, 3, 12} (chunks 0..5), TMA {13, 14} (chunks 6..8).
+  // Producer warps: load/store unit {0, 2, 3, 12}; TMA {13, 14} (contiguous runs).
   const int lsu = warp == 0 ? 0 : warp == 2 ? 1 : warp == 3 ? 2 : warp == 12 ? 3 : -1;
   const int tma = warp == 13 ? 0 : warp == 14 ? 1 : -1;
   if (warp == kLoaderWarp) {
-    index_loader(a, it, sm, c, false);
+    index_loader(a, it, sm, c);
   } else if (lsu >= 0) {
     constexpr int G = 16 / kLsuWarps;  // groups of four keys per warp (of the half's 16)
     for (int t = 0; t < it.ntiles; ++t) {
-      const int s = t & 1;
       if (!wait_ring(a, c, t)) break;
       const int* keys = ring_tile(sm, t) + HALF * half;
       const bool contig = c->icontig[t % NIDX] != 0;
@@ -404,32 +381,30 @@ __device__ void scorer(const VerifyArgs& a, const PoolMaps& maps, const Item& it
       for (int j = 0; j < G; ++j) ids[j] = keys[4 * (G * lsu + j) + (lane >> 3)];
       release_ring(c, t, lane);
       bool ok = true;
-      if (lane == 0) ok = wait_clu(&c->empty[s], ((t >> 1) & 1) ^ 1, c, a.status);
-      if (!__shfl_sync(0xffffffffu, ok, 0)) break;
-      uint8_t* slot = sm + Q_RING + s * KSLOT;
-      if (!contig) {  // a contiguous tile comes whole by TMA
+      for (int u = 0; u < 3 && ok; ++u) {
+        const int n = 3 * t + u, slot = n % QSLOTS;
+        if (lane == 0) ok = wait_clu(&c->empty[slot], ((n / QSLOTS) & 1) ^ 1, c, a.status);
+        ok = __shfl_sync(0xffffffffu, ok, 0);
+        if (!ok) break;
+        uint8_t* unit = sm + Q_RING + slot * QUNIT;
+        if (!contig) {  // a contiguous tile comes by TMA
 #pragma unroll 1
-        for (int ch = 0; ch < kScorerLsuChunks; ++ch)
-          lsu_chunk<G>(a.kv_pool, slot + ch * SCHUNK, ch, 4 * G * lsu, ids, lane);
+          for (int cc = 0; cc < 3; ++cc) lsu_chunk<G>(a.kv_pool, unit + cc * SCHUNK, 3 * u + cc, 4 * G * lsu, ids, lane);
+        }
+        cp_async_mbar_arrive(&c->full[slot]);
       }
-      cp_async_mbar_arrive(&c->full[s]);
+      if (!ok) break;
     }
     asm volatile("cp.async.wait_all;" ::: "memory");
   } else if (tma >= 0) {
-    constexpr int G = 16 / kTmaWarps;
-    tma_producer(a, it, c, tma, lane, [&](int t, uint64_t* bar) {
-      const int s = t & 1;
-      const int* keys = ring_tile(sm, t) + HALF * half;
-      uint8_t* slot = sm + Q_RING + s * KSLOT;
-      if (c->icontig[t % NIDX]) {
-        mbar_arrive_expect_tx(bar, tma == 0 ? KSLOT : 0);
-        if (tma == 0)
-          for (int ch = 0; ch < 9; ++ch)
-            tma_run(&maps.half, slot + ch * SCHUNK, ch, c->ifirst[t % NIDX] + HALF * half, bar);
-      } else {
-        mbar_arrive_expect_tx(bar, (9 - kScorerLsuChunks) * G * 512);
-        for (int ch = kScorerLsuChunks; ch < 9; ++ch) tma_gather(maps, slot + ch * SCHUNK, ch, keys, G * tma, G, bar);
-      }
+    tma_producer(a, it, c, tma, lane, 3, QSLOTS, [&](int n, int t, int u, int slot, uint64_t* bar) {
+      (void)n;
+      uint8_t* unit = sm + Q_RING + slot * QUNIT;
+      const bool load = c->icontig[t % NIDX] && tma == 0;
+      mbar_arrive_expect_tx(bar, load ? QUNIT : 0);
+      if (load)
+        for (int cc = 0; cc < 3; ++cc)
+          tma_run(&maps.half, unit + cc * SCHUNK, 3 * u + cc, c->ifirst[t % NIDX] + HALF * half, bar);
     });
   } else if (warp == 1 && lane == 0) {
     if (leader) {
@@ -440,35 +415,43 @@ __device__ void scorer(const VerifyArgs& a, const PoolMaps& maps, const Item& it
       tc_fence_after();
       for (int t = 0; t < it.ntiles && ok; ++t) {
         const int s = t & 1;
-        const uint32_t ph = (t >> 1) & 1;
         const uint32_t sbuf = tmem + 256 + 128 * s;
-        if (!wait_clu(&c->sempty[s], ph ^ 1, c, a.status) || !wait_cta(&c->full[s], ph, c, a.status) ||
-            !wait_clu(&c->peer[s], ph, c, a.status))
-          break;
+        ok = wait_clu(&c->sempty[s], ((t >> 1) & 1) ^ 1, c, a.status);
+        for (int u = 0; u < 3 && ok; ++u) {
+          const int n = 3 * t + u, slot = n % QSLOTS;
+          const uint32_t ph = (n / QSLOTS) & 1;
+          ok = wait_cta(&c->full[slot], ph, c, a.status) && wait_clu(&c->peer[slot], ph, c, a.status);
+        }
+        if (!ok) break;
         fence_async_smem();  // cp.async (generic proxy) data -> tensor-core reads
         tc_fence_after();
-        const uint8_t* slot = sm + Q_RING + s * KSLOT;
 #pragma unroll
-        for (int ch = 0; ch < 9; ++ch) {  // chunk ch: K steps 4ch .. 4ch+3 of the 36
-          const uint64_t kdesc = desc_sw128(smem_u32(slot + ch * SCHUNK), 16, 1024);
-          if (ch < 8) mma2_ts_x4(sbuf, tmem + ch * 32, kdesc, idesc, ch > 0);  // latent: Q from TMEM
-          else mma2_ss_x4<2, 2>(sbuf, rope_desc, kdesc, idesc, 1);            // rope: Q from shared memory
+        for (int u = 0; u < 3; ++u) {
+          const int slot = (3 * t + u) % QSLOTS;
+          const uint8_t* unit = sm + Q_RING + slot * QUNIT;
+#pragma unroll
+          for (int cc = 0; cc < 3; ++cc) {  // chunk ch = 3u + cc: K steps 4ch .. 4ch+3 of the 36
+            const int ch = 3 * u + cc;
+            const uint64_t kdesc = desc_sw128(smem_u32(unit + cc * SCHUNK), 16, 1024);
+            if (ch < 8) mma2_ts_x4(sbuf, tmem + ch * 32, kdesc, idesc, ch > 0);  // latent: Q from TMEM
+            else mma2_ss_x4<2, 2>(sbuf, rope_desc, kdesc, idesc, 1);            // rope: Q from shared memory
+          }
+          commit2(&c->empty[slot], kScorerPair);
         }
-        commit2(&c->empty[s], kScorerPair);
         commit2(&c->sfull[s], kScorerPair);
       }
       commit2(&c->mma_done, kScorerPair);
     } else {
-      // ---- follower: forward "my slot of tile t is full" to the leader
+      // ---- follower: forward "my unit n is full" to the leader
       const uint32_t lead_peer = map_cluster(smem_u32(&c->peer[0]), rank - 1);
       // The leader's MMAs read this CTA's Q too: it must be in place before
       // the first forward.
       if (!wait_clu(&c->q_ready, 0, c, a.status)) return;
-      for (int t = 0; t < it.ntiles; ++t) {
-        const int s = t & 1;
-        if (!wait_cta(&c->full[s], (t >> 1) & 1, c, a.status)) return;
+      for (int n = 0; n < 3 * it.ntiles; ++n) {
+        const int slot = n % QSLOTS;
+        if (!wait_cta(&c->full[slot], (n / QSLOTS) & 1, c, a.status)) return;
         fence_async_smem();
-        signal_remote(lead_peer + s * 8);
+        signal_remote(lead_peer + slot * 8);
       }
     }
   } else if (warp >= 4 && warp < 12) {
@@ -635,12 +618,12 @@ __device__ void accumulator(const VerifyArgs& a, const PoolMaps& maps, const Ite
   const bool leader = (rank & 1) == 0;
   const int par = rank & 1;            // value chunks 2q + par of every tile
   const uint32_t scorer_rank = rank - 2;
-  // Producer warps: load/store unit {0, 3, 8, 9} (q = 0..2), TMA {10, 11} (q = 3).
+  // Producer warps: load/store unit {0, 3, 8, 9}; TMA {10, 11} (contiguous runs).
   const int lsu = warp == 0 ? 0 : warp == 3 ? 1 : warp == 8 ? 2 : warp == 9 ? 3 : -1;
   const int tma = warp == 10 ? 0 : warp == 11 ? 1 : -1;
 
   if (warp == kLoaderWarp) {
-    index_loader(a, it, sm, c, true);
+    index_loader(a, it, sm, c);
   } else if (lsu >= 0) {
     constexpr int G = 32 / kLsuWarps;  // groups of four keys per warp (of the tile's 32)
     for (int t = 0; t < it.ntiles; ++t) {
@@ -658,25 +641,20 @@ __device__ void accumulator(const VerifyArgs& a, const PoolMaps& maps, const Ite
       uint8_t* slot = sm + V_RING + s * VSLOT;
       if (!contig) {
 #pragma unroll 1
-        for (int q = 0; q < kAccLsuChunks; ++q) lsu_chunk<G>(a.kv_pool, slot + q * VCHUNK, 2 * q + par, 4 * G * lsu, ids, lane);
+        for (int q = 0; q < 4; ++q) lsu_chunk<G>(a.kv_pool, slot + q * VCHUNK, 2 * q + par, 4 * G * lsu, ids, lane);
       }
       cp_async_mbar_arrive(&c->full[s]);
     }
     asm volatile("cp.async.wait_all;" ::: "memory");
   } else if (tma >= 0) {
-    constexpr int G = 32 / kTmaWarps;
-    tma_producer(a, it, c, tma, lane, [&](int t, uint64_t* bar) {
-      const int s = t & 1;
-      const int* keys = ring_tile(sm, t);
-      uint8_t* slot = sm + V_RING + s * VSLOT;
-      if (c->icontig[t % NIDX]) {
-        mbar_arrive_expect_tx(bar, tma == 0 ? VSLOT : 0);
-        if (tma == 0)
-          for (int q = 0; q < 4; ++q) tma_run(&maps.tile, slot + q * VCHUNK, 2 * q + par, c->ifirst[t % NIDX], bar);
-      } else {
-        mbar_arrive_expect_tx(bar, (4 - kAccLsuChunks) * G * 512);
-        for (int q = kAccLsuChunks; q < 4; ++q) tma_gather(maps, slot + q * VCHUNK, 2 * q + par, keys, G * tma, G, bar);
-      }
+    tma_producer(a, it, c, tma, lane, 1, VSLOTS, [&](int n, int t, int u, int slot, uint64_t* bar) {
+      (void)n;
+      (void)u;
+      uint8_t* dst = sm + V_RING + slot * VSLOT;
+      const bool load = c->icontig[t % NIDX] && tma == 0;
+      mbar_arrive_expect_tx(bar, load ? VSLOT : 0);
+      if (load)
+        for (int q = 0; q < 4; ++q) tma_run(&maps.tile, dst + q * VCHUNK, 2 * q + par, c->ifirst[t % NIDX], bar);
     });
   } else if (warp == 1 && lane == 0) {
     if (leader) {
@@ -852,7 +830,7 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(kThreads, 1)
 
   if (rank < 2 && have && tid < a.n_nodes) c->par[tid] = __ldg(a.tree_parent + (size_t)it.loc.b * a.n_nodes + tid);
   if (tid == 0) {
-    for (int i = 0; i < 2; ++i) {
+    for (int i = 0; i < kMaxSlots; ++i) {
       mbar_init(&c->full[i], 32 * kLsuWarps + kTmaWarps);  // every producer lane, each TMA warp once
       mbar_init(&c->peer[i], 1);
       mbar_init(&c->empty[i], 1);
@@ -966,7 +944,7 @@ EncodeTiledFn encode_fn() {
 
 // Pool maps over [rows, 576] bf16 with 1152-byte rows, 128-byte swizzle:
 // `tile` has a 128-row box (a whole tile), `half` a 64-row box (one scorer
-// half), `row` a 1-row box (gather4).  Rows past the pool read as zeros; with
+// half).  Rows past the pool read as zeros; with
 // an unknown pool size the row extent is the int32 index range (the caller
 // vouches for the indices).
 cudaError_t make_pool_maps(const VerifyArgs& a, PoolMaps* m) {
@@ -975,12 +953,12 @@ cudaError_t make_pool_maps(const VerifyArgs& a, PoolMaps* m) {
   const cuuint64_t rows = a.pool_rows > 0 ? (cuuint64_t)a.pool_rows : (cuuint64_t)0x7fffffff;
   const cuuint64_t dims[2] = {(cuuint64_t)kRow, rows};
   const cuuint64_t strides[1] = {(cuuint64_t)kRow * 2};
-  const cuuint32_t box_half[2] = {64, (cuuint32_t)HALF}, box_tile[2] = {64, (cuuint32_t)TK}, box_row[2] = {64, 1};
+  const cuuint32_t box_half[2] = {64, (cuuint32_t)HALF}, box_tile[2] = {64, (cuuint32_t)TK};
   const cuuint32_t es[2] = {1, 1};
   void* base = const_cast<uint16_t*>(a.kv_pool);
-  const cuuint32_t* boxes[3] = {box_half, box_tile, box_row};
-  CUtensorMap* maps[3] = {&m->half, &m->tile, &m->row};
-  for (int i = 0; i < 3; ++i)
+  const cuuint32_t* boxes[2] = {box_half, box_tile};
+  CUtensorMap* maps[2] = {&m->half, &m->tile};
+  for (int i = 0; i < 2; ++i)
     if (enc(maps[i], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, base, dims, strides, boxes[i], es,
             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
