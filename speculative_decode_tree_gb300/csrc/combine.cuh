@@ -52,8 +52,10 @@ __device__ __forceinline__ void combine_unit(const VerifyArgs& a, int u, int lan
 #pragma unroll
     for (int j = 0; j < kCombineBatch; ++j) {
       const bool in = s0 + j < count;
-      ls[j] = in ? __ldg(pl + (size_t)(s0 + j) * rows) : -INFINITY;
-      x[j] = in ? __ldg(reinterpret_cast<const uint32_t*>(po + (size_t)(s0 + j) * o_stride)) : 0u;
+      // L2-coherent loads: in the fused form the partials were written by
+      // other CTAs of the same launch.
+      ls[j] = in ? __ldcg(pl + (size_t)(s0 + j) * rows) : -INFINITY;
+      x[j] = in ? __ldcg(reinterpret_cast<const uint32_t*>(po + (size_t)(s0 + j) * o_stride)) : 0u;
     }
     float bm = m;
 #pragma unroll

@@ -3,7 +3,7 @@
 //
 // Combine: per query row, lse = ln sum_s exp(lse_s) and
 // O = sum_s exp(lse_s - lse) * O_s over the request's splits, written as bf16
-// (round to nearest even) plus the fp32 lse.  One warp per (row, 128 output
+// (round to nearest even) plus the fp32 lse.  One warp per (row, 64 output
 // columns); the merge itself is combine_unit (combine.cuh), shared with the
 // partial kernel that merges its own splits.
 #include "combine.cuh"

@@ -30,10 +30,11 @@
 // unit warps copy the scattered 1152-byte rows as 64-column chunks with
 // 16-byte cp.async (measured faster per SM than TMA gather4 for these rows);
 // a tile whose 128 indices form one contiguous run comes by 2-D TMA tile
-// loads instead.  A TMA warp's loads complete on its own barriers (one lane
-// issues, another lane waits for each unit's bytes and then counts the warp
-// in), so every load a CTA issued is known to have landed before it exits,
-// also after an expired wait.  The scorer's key ring holds seven units of
+// loads instead.  TMA loads complete on the stream's own barriers (one warp
+// issues, a second warp waits for each unit's bytes and then counts the
+// stream in), so every load a CTA issued is known to have landed before it
+// exits, also after an expired wait.  No warp runs two spinning roles: a lane
+// suspended in a barrier wait holds back every other lane of its warp.  The scorer's key ring holds seven units of
 // three chunks (2.3 tiles), enough to keep the next tile's rows in flight
 // while a tile is multiplied.  The follower CTA of each pair forwards "my
 // unit is complete" to the leader, whose MMA thread waits for a whole tile
@@ -75,7 +76,6 @@ constexpr int PBUF = 34816;              // P buffer stride (1024-aligned)
 constexpr int NIDX = 8;                  // index ring: tiles of indices held ahead
 constexpr int kThreads = 512;            // 16 warps
 constexpr int kLsuWarps = 4;             // producer warps on the load/store unit (cp.async)
-constexpr int kTmaWarps = 2;             // producer warps issuing TMA loads
 constexpr int kLoaderWarp = 15;
 constexpr float kLazyRescale = 8.0f;     // rescale only when the max grows by > 2^8 (log2 units)
 // Tensor-core work must be complete before TMEM is freed: this wait keeps a
@@ -97,12 +97,12 @@ constexpr int BIG_END = IDX_RING + NIDX * TK * 4;
 
 struct __align__(8) Ctrl {
   // Ring slot barriers (per unit slot): full = this CTA's chunks of the unit
-  // landed (every producer lane + each TMA warp once), peer = (leader) the
-  // follower's slot is full, empty = the pair's MMAs consumed the slot
-  // (commit multicast to both CTAs of the pair); tma = each TMA warp's own
+  // landed (every load/store-unit lane + the TMA forwarder), peer = (leader)
+  // the follower's slot is full, empty = the pair's MMAs consumed the slot
+  // (commit multicast to both CTAs of the pair); tma = the TMA stream's
   // loads of the unit landed.
-  uint64_t full[kMaxSlots], peer[kMaxSlots], empty[kMaxSlots], tma[kTmaWarps][kMaxSlots];
-  uint32_t tma_issued[kTmaWarps];  // units whose TMA loads a warp has issued
+  uint64_t full[kMaxSlots], peer[kMaxSlots], empty[kMaxSlots], tma[kMaxSlots];
+  uint32_t tma_issued;  // units whose TMA loads the issuer has started (bit 31: done)
   // scorer
   uint64_t sfull[2], sempty[2], pfree[2];
   // accumulator
@@ -311,49 +311,54 @@ __device__ __forceinline__ void tma_run(const CUtensorMap* map, uint8_t* dst, in
       : "memory");
 }
 
-// A TMA producer warp over a ring of `nslots` unit slots, `upt` units per
-// tile.  Lane 0 issues each unit's loads once its slot is free
-// (`issue(n, t, u, slot, bar)` arms the warp's barrier `bar` with the unit's
-// bytes -- possibly none -- and starts them); lane 1 waits for each issued
-// unit's bytes and then counts the warp in on the slot's full barrier.  After
-// an expired wait lane 1 still waits (fixed bound) for every unit lane 0
-// issued, so no load is in flight when the CTA leaves.
+// The TMA stream of a CTA over a ring of `nslots` unit slots, `upt` units
+// per tile, run by two warps (lane 0 of each).  The issuer starts each unit's
+// loads once its slot is free: `issue(n, t, u, slot, bar)` arms the stream's
+// barrier `bar` with the unit's bytes -- possibly none -- and starts them.  The
+// forwarder waits for each issued unit's bytes and then counts the stream in
+// on the slot's full barrier.  They are separate warps because a lane
+// suspended in a barrier wait holds back the other lanes of its warp: an
+// issuer waiting for a slot that only frees once a landed unit is forwarded
+// would stall its own forwarder.  After an expired wait the forwarder still
+// waits (fixed bound) for every unit the issuer started, so no load is in
+// flight when the CTA leaves.
 template <typename Issue>
-__device__ __forceinline__ void tma_producer(const VerifyArgs& a, const Item& it, Ctrl* c, int w, int lane,
-                                             int upt, int nslots, Issue&& issue) {
-  volatile uint32_t* issued = &c->tma_issued[w];
+__device__ __forceinline__ void tma_issuer(const VerifyArgs& a, const Item& it, Ctrl* c, int upt, int nslots,
+                                           Issue&& issue) {
+  volatile uint32_t* issued = &c->tma_issued;
   const int nunits = it.ntiles * upt;
-  if (lane == 0) {
-    for (int n = 0; n < nunits; ++n) {
-      const int t = n / upt, u = n - t * upt, slot = n % nslots;
-      if (u == 0 && !wait_ring(a, c, t)) break;
-      const bool free = wait_clu(&c->empty[slot], ((n / nslots) & 1) ^ 1, c, a.status);
-      if (free) issue(n, t, u, slot, &c->tma[w][slot]);
-      if (!free || u == upt - 1) mbar_arrive(&c->iempty[t % NIDX]);
-      if (!free) break;
-      __threadfence_block();
-      *issued = (uint32_t)(n + 1);
-    }
+  for (int n = 0; n < nunits; ++n) {
+    const int t = n / upt, u = n - t * upt, slot = n % nslots;
+    if (u == 0 && !wait_ring(a, c, t)) break;
+    const bool free = wait_clu(&c->empty[slot], ((n / nslots) & 1) ^ 1, c, a.status);
+    if (free) issue(n, t, u, slot, &c->tma[slot]);
+    if (!free || u == upt - 1) mbar_arrive(&c->iempty[t % NIDX]);
+    if (!free) break;
     __threadfence_block();
-    *issued = *issued | 0x80000000u;  // done issuing
-  } else if (lane == 1) {
-    for (int n = 0; n < nunits; ++n) {
-      // Wait (bounded) until lane 0 issued unit n or stopped.
-      uint32_t v = *issued;
-      const uint64_t deadline = global_timer_ns() + kDrainNs;
-      while ((v & 0x7fffffffu) <= (uint32_t)n && !(v & 0x80000000u) && global_timer_ns() < deadline) {
-        __nanosleep(32);
-        v = *issued;
-      }
-      if ((v & 0x7fffffffu) <= (uint32_t)n) break;  // never issued
-      const int slot = n % nslots;
-      if (!mbar_wait(&c->tma[w][slot], (n / nslots) & 1, global_timer_ns() + kDrainNs)) {
-        atomicOr(a.status, DDTREE_ST_TIMEOUT);
-        c->abort = 1;
-        break;
-      }
-      mbar_arrive(&c->full[slot]);
+    *issued = (uint32_t)(n + 1);
+  }
+  __threadfence_block();
+  *issued = *issued | 0x80000000u;  // done issuing
+}
+__device__ __forceinline__ void tma_forwarder(const VerifyArgs& a, const Item& it, Ctrl* c, int upt, int nslots) {
+  volatile uint32_t* issued = &c->tma_issued;
+  const int nunits = it.ntiles * upt;
+  for (int n = 0; n < nunits; ++n) {
+    // Wait (bounded) until the issuer started unit n or stopped.
+    uint32_t v = *issued;
+    const uint64_t deadline = global_timer_ns() + kDrainNs;
+    while ((v & 0x7fffffffu) <= (uint32_t)n && !(v & 0x80000000u) && global_timer_ns() < deadline) {
+      __nanosleep(32);
+      v = *issued;
     }
+    if ((v & 0x7fffffffu) <= (uint32_t)n) break;  // never issued
+    const int slot = n % nslots;
+    if (!mbar_wait(&c->tma[slot], (n / nslots) & 1, global_timer_ns() + kDrainNs)) {
+      atomicOr(a.status, DDTREE_ST_TIMEOUT);
+      c->abort = 1;
+      break;
+    }
+    mbar_arrive(&c->full[slot]);
   }
 }
 
@@ -365,9 +370,9 @@ __device__ void scorer(const VerifyArgs& a, const PoolMaps& maps, const Item& it
   const bool leader = (rank & 1) == 0;
   const int half = rank & 1;           // which 64 keys of each tile this CTA gathers
 
-  // Producer warps: load/store unit {0, 2, 3, 12}; TMA {13, 14} (contiguous runs).
+  // Producer warps: load/store unit {0, 2, 3, 12}; TMA issuer 13 and
+  // forwarder 14 (contiguous runs).
   const int lsu = warp == 0 ? 0 : warp == 2 ? 1 : warp == 3 ? 2 : warp == 12 ? 3 : -1;
-  const int tma = warp == 13 ? 0 : warp == 14 ? 1 : -1;
   if (warp == kLoaderWarp) {
     index_loader(a, it, sm, c);
   } else if (lsu >= 0) {
@@ -396,16 +401,18 @@ __device__ void scorer(const VerifyArgs& a, const PoolMaps& maps, const Item& it
       if (!ok) break;
     }
     asm volatile("cp.async.wait_all;" ::: "memory");
-  } else if (tma >= 0) {
-    tma_producer(a, it, c, tma, lane, 3, QSLOTS, [&](int n, int t, int u, int slot, uint64_t* bar) {
+  } else if (warp == 13 && lane == 0) {
+    tma_issuer(a, it, c, 3, QSLOTS, [&](int n, int t, int u, int slot, uint64_t* bar) {
       (void)n;
       uint8_t* unit = sm + Q_RING + slot * QUNIT;
-      const bool load = c->icontig[t % NIDX] && tma == 0;
+      const bool load = c->icontig[t % NIDX] != 0;
       mbar_arrive_expect_tx(bar, load ? QUNIT : 0);
       if (load)
         for (int cc = 0; cc < 3; ++cc)
           tma_run(&maps.half, unit + cc * SCHUNK, 3 * u + cc, c->ifirst[t % NIDX] + HALF * half, bar);
     });
+  } else if (warp == 14 && lane == 0) {
+    tma_forwarder(a, it, c, 3, QSLOTS);
   } else if (warp == 1 && lane == 0) {
     if (leader) {
       // ---- MMA issuer for the pair: one tile at a time, once all of it landed
@@ -618,9 +625,9 @@ __device__ void accumulator(const VerifyArgs& a, const PoolMaps& maps, const Ite
   const bool leader = (rank & 1) == 0;
   const int par = rank & 1;            // value chunks 2q + par of every tile
   const uint32_t scorer_rank = rank - 2;
-  // Producer warps: load/store unit {0, 3, 8, 9}; TMA {10, 11} (contiguous runs).
+  // Producer warps: load/store unit {0, 3, 8, 9}; TMA issuer 10 and
+  // forwarder 11 (contiguous runs).
   const int lsu = warp == 0 ? 0 : warp == 3 ? 1 : warp == 8 ? 2 : warp == 9 ? 3 : -1;
-  const int tma = warp == 10 ? 0 : warp == 11 ? 1 : -1;
 
   if (warp == kLoaderWarp) {
     index_loader(a, it, sm, c);
@@ -646,16 +653,18 @@ __device__ void accumulator(const VerifyArgs& a, const PoolMaps& maps, const Ite
       cp_async_mbar_arrive(&c->full[s]);
     }
     asm volatile("cp.async.wait_all;" ::: "memory");
-  } else if (tma >= 0) {
-    tma_producer(a, it, c, tma, lane, 1, VSLOTS, [&](int n, int t, int u, int slot, uint64_t* bar) {
+  } else if (warp == 10 && lane == 0) {
+    tma_issuer(a, it, c, 1, VSLOTS, [&](int n, int t, int u, int slot, uint64_t* bar) {
       (void)n;
       (void)u;
       uint8_t* dst = sm + V_RING + slot * VSLOT;
-      const bool load = c->icontig[t % NIDX] && tma == 0;
+      const bool load = c->icontig[t % NIDX] != 0;
       mbar_arrive_expect_tx(bar, load ? VSLOT : 0);
       if (load)
         for (int q = 0; q < 4; ++q) tma_run(&maps.tile, dst + q * VCHUNK, 2 * q + par, c->ifirst[t % NIDX], bar);
     });
+  } else if (warp == 11 && lane == 0) {
+    tma_forwarder(a, it, c, 1, VSLOTS);
   } else if (warp == 1 && lane == 0) {
     if (leader) {
       // ---- MMA issuer for the pair: O[rows, 128q .. 128q+127] += P V
@@ -831,12 +840,12 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(kThreads, 1)
   if (rank < 2 && have && tid < a.n_nodes) c->par[tid] = __ldg(a.tree_parent + (size_t)it.loc.b * a.n_nodes + tid);
   if (tid == 0) {
     for (int i = 0; i < kMaxSlots; ++i) {
-      mbar_init(&c->full[i], 32 * kLsuWarps + kTmaWarps);  // every producer lane, each TMA warp once
+      mbar_init(&c->full[i], 32 * kLsuWarps + 1);  // every load/store-unit lane, the TMA forwarder
       mbar_init(&c->peer[i], 1);
       mbar_init(&c->empty[i], 1);
-      for (int w = 0; w < kTmaWarps; ++w) mbar_init(&c->tma[w][i], 1);
+      mbar_init(&c->tma[i], 1);
     }
-    for (int w = 0; w < kTmaWarps; ++w) c->tma_issued[w] = 0;
+    c->tma_issued = 0;
     for (int i = 0; i < 2; ++i) {
       mbar_init(&c->sfull[i], 1);
       mbar_init(&c->sempty[i], 16);
@@ -850,7 +859,7 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(kThreads, 1)
     // producer warp, and in the scorers also by the eight softmax warps.
     for (int i = 0; i < NIDX; ++i) {
       mbar_init(&c->ifull[i], 32);
-      mbar_init(&c->iempty[i], kLsuWarps + kTmaWarps + (rank < 2 ? 8 : 0));
+      mbar_init(&c->iempty[i], kLsuWarps + 1 + (rank < 2 ? 8 : 0));
     }
     mbar_init(&c->mma_done, 1);
     mbar_init(&c->q_ready, 8);
@@ -895,7 +904,7 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(kThreads, 1)
     // Merge the splits in this launch: every CTA of the grid is resident at
     // once (cooperative launch), so each counts itself done and waits,
     // bounded, for all others; then the warps of the grid share the
-    // (row, 128-column) merge units.  A timed-out wait anywhere writes zeros.
+    // (row, 64-column) merge units.  A timed-out wait anywhere writes zeros.
     if (tid == 0) {
       __threadfence();
       atomicAdd(a.grid_done, 1u);
