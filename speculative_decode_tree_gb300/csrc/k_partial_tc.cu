@@ -91,14 +91,14 @@ __device__ __forceinline__ void set_abort(Ctrl* c, uint32_t* status) {
 // Bounded wait; on expiry mark the CTA aborted.  Returns false when aborted.
 __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, Ctrl* c, uint32_t* status) {
   if (*(volatile uint32_t*)&c->abort) return false;
-  if (mbar_wait(bar, parity, global_timer_ns() + kWaitNs)) return true;
+  if (mbar_wait(bar, parity, kWaitNs)) return true;
   set_abort(c, status);
   return false;
 }
 __device__ __forceinline__ bool wait_cluster_or_abort(uint64_t* bar, uint32_t parity, Ctrl* c,
                                                       uint32_t* status) {
   if (*(volatile uint32_t*)&c->abort) return false;
-  if (mbar_wait_cluster(bar, parity, global_timer_ns() + kWaitNs)) return true;
+  if (mbar_wait_cluster(bar, parity, kWaitNs)) return true;
   set_abort(c, status);
   return false;
 }
@@ -670,7 +670,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   __syncthreads();
   // Tensor-core work of this CTA must be finished before TMEM is freed.
   if (warp == 3 && have && it.ntiles > 0) {
-    mbar_wait(&c->mma_done, 0, global_timer_ns() + kWaitNs);
+    mbar_wait(&c->mma_done, 0, kWaitNs);
   }
   tc_fence_before();
   __syncthreads();

@@ -88,6 +88,14 @@ constexpr int Q_ROPE = 0;                               // scorer: 16 KB
 constexpr int Q_RING = Q_ROPE + VCHUNK;                 // scorer: 7 x 24 KB
 constexpr int Q_STAGE = Q_RING + QSLOTS * QUNIT;        // scorer: P staging
 constexpr int Q_END = Q_STAGE + PBUF;
+// Q latent (128 rows x 512 bf16, eight 64-column 128-byte-swizzled boxes)
+// lands by TMA in ring slots 2.. and the start of the P staging buffer,
+// before any of them is used; the softmax warps move it into TMEM.
+constexpr int Q_LAT_STAGE = Q_RING + 2 * QUNIT;
+constexpr int Q_LAT_BYTES = ROWS * kLatent * 2;
+constexpr int Q_ROPE_BYTES = ROWS * kRope * 2;
+static_assert(Q_LAT_STAGE + Q_LAT_BYTES <= Q_END, "Q latent staging fits the unused ring");
+static_assert(Q_LAT_STAGE % 1024 == 0, "128-byte swizzle wants 1024-byte aligned boxes");
 constexpr int V_PBUF = 0;                               // accumulator: 2 x PBUF
 constexpr int V_RING = V_PBUF + 2 * PBUF;               // accumulator: 2 x 64 KB
 constexpr int V_END = V_RING + VSLOTS * VSLOT;
@@ -106,13 +114,14 @@ struct __align__(8) Ctrl {
   // scorer
   uint64_t sfull[2], sempty[2], pfree[2];
   // accumulator
-  uint64_t pfull[2], ppeer[2], pvdone[2], corr_done[2];
+  uint64_t pfull[2], pvdone[2], corr_done[2];
   // both
   uint64_t ifull[NIDX], iempty[NIDX];  // index ring
   int32_t ifirst[NIDX];    // first index of each ring tile
   int32_t icontig[NIDX];   // the tile's 128 indices form one run
   uint64_t mma_done;
   uint64_t q_ready;   // scorer: Q latent in TMEM and Q rope in shared memory
+  uint64_t qload;     // scorer: the TMA loads of Q (latent staging + rope) landed
   uint64_t wait_ns;        // bound of the waits (the caller's, default 2 s)
   uint32_t tmem_base;
   uint32_t abort;
@@ -130,19 +139,15 @@ __device__ __forceinline__ void set_abort(Ctrl* c, uint32_t* status) {
   c->abort = 1;
   atomicOr(status, DDTREE_ST_TIMEOUT);
 }
-// Bounded wait with cluster-scope acquire (most barriers here are arrived on
-// by another CTA: peer forwards, multicast commits, bulk-copy completions);
-// on expiry mark the CTA aborted.  False when aborted.
-__device__ __forceinline__ bool wait_clu(uint64_t* bar, uint32_t parity, Ctrl* c, uint32_t* status) {
+// Bounded wait on a barrier phase; on expiry mark the CTA aborted.  False
+// when aborted.  CTA-scope acquire also for the barriers that other CTAs of
+// the cluster arrive on: what they announce is tensor-core, bulk-copy or
+// cp.async work whose completion the barrier itself tracks (or a forward of
+// such a completion), not generic stores of the remote thread; a
+// cluster-scope acquire measured slower on these per-unit waits.
+__device__ __forceinline__ bool wait_bar(uint64_t* bar, uint32_t parity, Ctrl* c, uint32_t* status) {
   if (aborted(c)) return false;
-  if (mbar_wait_cluster(bar, parity, global_timer_ns() + c->wait_ns)) return true;
-  set_abort(c, status);
-  return false;
-}
-// Same, CTA scope (barriers arrived on by this CTA's own threads).
-__device__ __forceinline__ bool wait_cta(uint64_t* bar, uint32_t parity, Ctrl* c, uint32_t* status) {
-  if (aborted(c)) return false;
-  if (mbar_wait(bar, parity, global_timer_ns() + c->wait_ns)) return true;
+  if (mbar_wait(bar, parity, c->wait_ns)) return true;
   set_abort(c, status);
   return false;
 }
@@ -235,7 +240,22 @@ struct PoolMaps {
   CUtensorMap half;   // 64 columns x 64 rows box: a scorer's half of a contiguous tile
   CUtensorMap tile;   // 64 columns x 128 rows box: an accumulator chunk of a contiguous tile
   CUtensorMap po;     // partial O [splits][rows_per_req][512] bf16, 64 columns x 128 rows box
+  CUtensorMap ql;     // Q latent [B*T*H rows][512] bf16, 64 columns x 128 rows box
+  CUtensorMap qr;     // Q rope [B*T*H rows][64] bf16, 64 columns x 128 rows box
 };
+
+// The start-of-kernel cluster barrier is split: every thread arrives once its
+// CTA's barriers and TMEM are set up, and a thread waits for the other CTAs
+// only before its first remote action (an arrive on, a copy to, or an MMA
+// reading another CTA).  Producers that touch only their own CTA start at
+// once.  Every thread waits exactly once (the kernel waits for those that did
+// not) before the closing cluster barrier.
+__device__ __forceinline__ void join_cluster(bool& joined) {
+  if (!joined) {
+    asm volatile("barrier.cluster.wait.acquire;" ::: "memory");
+    joined = true;
+  }
+}
 
 // ------------------------------------------------------------ index ring
 __device__ __forceinline__ int* ring_tile(uint8_t* sm, int t) {
@@ -243,43 +263,55 @@ __device__ __forceinline__ int* ring_tile(uint8_t* sm, int t) {
 }
 
 // Loader warp: tile j's 128 indices (invalid ones -> -1, flagged) into ring
-// slot j % NIDX, with the tile's first index and whether it is one run.  (An
-// L2 prefetch of the rows from this warp measured slower: the prefetch
-// instructions held the loader back.)
+// slot j % NIDX, with the tile's first index and whether it is one run.  The
+// loads of four tiles are in flight together (the first tiles' latency is on
+// the critical path of the start).  (An L2 prefetch of the rows from this
+// warp measured slower: the prefetch instructions held the loader back.)
 __device__ void index_loader(const VerifyArgs& a, const Item& it, uint8_t* sm, Ctrl* c) {
+  constexpr int kBatch = 4;
   const int lane = threadIdx.x & 31;
-  for (int j = 0; j < it.ntiles; ++j) {
-    const int slot = j % NIDX;
-    if (j >= NIDX && !wait_cta(&c->iempty[slot], ((j / NIDX) - 1) & 1, c, a.status)) return;
-    const int k0 = it.k_begin + j * TK + 4 * lane;
-    int v[4];
+  for (int j0 = 0; j0 < it.ntiles; j0 += kBatch) {
+    int v[kBatch][4];
 #pragma unroll
-    for (int e = 0; e < 4; ++e) v[e] = (k0 + e < it.k_end) ? __ldg(a.kv_indices + it.loc.idx_base + k0 + e) : -1;
+    for (int jj = 0; jj < kBatch; ++jj) {
+      const int k0 = it.k_begin + (j0 + jj) * TK + 4 * lane;
 #pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      if (k0 + e < it.k_end && (v[e] < 0 || (a.pool_rows > 0 && v[e] >= a.pool_rows))) {
-        atomicOr(a.status, DDTREE_ST_BAD_INDEX);
-        v[e] = -1;
+      for (int e = 0; e < 4; ++e)
+        v[jj][e] = (j0 + jj < it.ntiles && k0 + e < it.k_end) ? __ldg(a.kv_indices + it.loc.idx_base + k0 + e) : -1;
+    }
+#pragma unroll
+    for (int jj = 0; jj < kBatch; ++jj) {
+      const int j = j0 + jj, slot = j % NIDX;
+      if (j >= it.ntiles) break;
+      if (j >= NIDX && !wait_bar(&c->iempty[slot], ((j / NIDX) - 1) & 1, c, a.status)) return;
+      const int k0 = it.k_begin + j * TK + 4 * lane;
+      int* w = v[jj];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        if (k0 + e < it.k_end && (w[e] < 0 || (a.pool_rows > 0 && w[e] >= a.pool_rows))) {
+          atomicOr(a.status, DDTREE_ST_BAD_INDEX);
+          w[e] = -1;
+        }
       }
+      int* dst = ring_tile(sm, j);
+      *reinterpret_cast<int4*>(dst + 4 * lane) = make_int4(w[0], w[1], w[2], w[3]);
+      const int first = __shfl_sync(0xffffffffu, w[0], 0);
+      const bool run = w[0] >= 0 && w[0] == first + 4 * lane && w[1] == w[0] + 1 && w[2] == w[0] + 2 &&
+                       w[3] == w[0] + 3;
+      const bool contig = __all_sync(0xffffffffu, run);
+      if (lane == 0) {
+        c->ifirst[slot] = first;
+        c->icontig[slot] = contig ? 1 : 0;
+      }
+      __syncwarp();
+      mbar_arrive(&c->ifull[slot]);  // 32 arrivals: every lane's stores are released
     }
-    int* dst = ring_tile(sm, j);
-    *reinterpret_cast<int4*>(dst + 4 * lane) = make_int4(v[0], v[1], v[2], v[3]);
-    const int first = __shfl_sync(0xffffffffu, v[0], 0);
-    const bool run = v[0] >= 0 && v[0] == first + 4 * lane && v[1] == v[0] + 1 && v[2] == v[0] + 2 &&
-                     v[3] == v[0] + 3;
-    const bool contig = __all_sync(0xffffffffu, run);
-    if (lane == 0) {
-      c->ifirst[slot] = first;
-      c->icontig[slot] = contig ? 1 : 0;
-    }
-    __syncwarp();
-    mbar_arrive(&c->ifull[slot]);  // 32 arrivals: every lane's stores are released
   }
 }
 
 // Waits until ring tile t is loaded (every lane acquires it).
 __device__ __forceinline__ bool wait_ring(const VerifyArgs& a, Ctrl* c, int t) {
-  return wait_cta(&c->ifull[t % NIDX], (t / NIDX) & 1, c, a.status);
+  return wait_bar(&c->ifull[t % NIDX], (t / NIDX) & 1, c, a.status);
 }
 __device__ __forceinline__ void release_ring(Ctrl* c, int t, int lane) {
   __syncwarp();
@@ -316,7 +348,8 @@ __device__ __forceinline__ void tma_run(const CUtensorMap* map, uint8_t* dst, in
 // loads once its slot is free: `issue(n, t, u, slot, bar)` arms the stream's
 // barrier `bar` with the unit's bytes -- possibly none -- and starts them.  The
 // forwarder waits for each issued unit's bytes and then counts the stream in
-// on the slot's full barrier.  They are separate warps because a lane
+// on the slot's full barrier.  A non-null `gate2` is waited for (phase 0)
+// before unit 2 is issued.  They are separate warps because a lane
 // suspended in a barrier wait holds back the other lanes of its warp: an
 // issuer waiting for a slot that only frees once a landed unit is forwarded
 // would stall its own forwarder.  After an expired wait the forwarder still
@@ -324,13 +357,14 @@ __device__ __forceinline__ void tma_run(const CUtensorMap* map, uint8_t* dst, in
 // flight when the CTA leaves.
 template <typename Issue>
 __device__ __forceinline__ void tma_issuer(const VerifyArgs& a, const Item& it, Ctrl* c, int upt, int nslots,
-                                           Issue&& issue) {
+                                           uint64_t* gate2, Issue&& issue) {
   volatile uint32_t* issued = &c->tma_issued;
   const int nunits = it.ntiles * upt;
   for (int n = 0; n < nunits; ++n) {
     const int t = n / upt, u = n - t * upt, slot = n % nslots;
     if (u == 0 && !wait_ring(a, c, t)) break;
-    const bool free = wait_clu(&c->empty[slot], ((n / nslots) & 1) ^ 1, c, a.status);
+    const bool free = (n != 2 || gate2 == nullptr || wait_bar(gate2, 0, c, a.status)) &&
+                      wait_bar(&c->empty[slot], ((n / nslots) & 1) ^ 1, c, a.status);
     if (free) issue(n, t, u, slot, &c->tma[slot]);
     if (!free || u == upt - 1) mbar_arrive(&c->iempty[t % NIDX]);
     if (!free) break;
@@ -346,14 +380,16 @@ __device__ __forceinline__ void tma_forwarder(const VerifyArgs& a, const Item& i
   for (int n = 0; n < nunits; ++n) {
     // Wait (bounded) until the issuer started unit n or stopped.
     uint32_t v = *issued;
-    const uint64_t deadline = global_timer_ns() + kDrainNs;
-    while ((v & 0x7fffffffu) <= (uint32_t)n && !(v & 0x80000000u) && global_timer_ns() < deadline) {
-      __nanosleep(32);
-      v = *issued;
+    if ((v & 0x7fffffffu) <= (uint32_t)n && !(v & 0x80000000u)) {
+      const uint64_t deadline = global_timer_ns() + kDrainNs;
+      while ((v & 0x7fffffffu) <= (uint32_t)n && !(v & 0x80000000u) && global_timer_ns() < deadline) {
+        __nanosleep(32);
+        v = *issued;
+      }
     }
     if ((v & 0x7fffffffu) <= (uint32_t)n) break;  // never issued
     const int slot = n % nslots;
-    if (!mbar_wait(&c->tma[slot], (n / nslots) & 1, global_timer_ns() + kDrainNs)) {
+    if (!mbar_wait(&c->tma[slot], (n / nslots) & 1, kDrainNs)) {
       atomicOr(a.status, DDTREE_ST_TIMEOUT);
       c->abort = 1;
       break;
@@ -364,7 +400,7 @@ __device__ __forceinline__ void tma_forwarder(const VerifyArgs& a, const Item& i
 
 // ------------------------------------------------------------------ scorer
 __device__ void scorer(const VerifyArgs& a, const PoolMaps& maps, const Item& it, uint8_t* sm, Ctrl* c,
-                       uint32_t rank) {
+                       uint32_t rank, bool& joined) {
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const uint32_t tmem = c->tmem_base;  // [0,256): Q latent; [256,384), [384,512): S
   const bool leader = (rank & 1) == 0;
@@ -388,7 +424,11 @@ __device__ void scorer(const VerifyArgs& a, const PoolMaps& maps, const Item& it
       bool ok = true;
       for (int u = 0; u < 3 && ok; ++u) {
         const int n = 3 * t + u, slot = n % QSLOTS;
-        if (lane == 0) ok = wait_clu(&c->empty[slot], ((n / QSLOTS) & 1) ^ 1, c, a.status);
+        // Slots 2.. hold the Q latent staging until the softmax warps moved
+        // it into TMEM (q_ready).
+        if (lane == 0)
+          ok = (n != 2 || wait_bar(&c->q_ready, 0, c, a.status)) &&
+               wait_bar(&c->empty[slot], ((n / QSLOTS) & 1) ^ 1, c, a.status);
         ok = __shfl_sync(0xffffffffu, ok, 0);
         if (!ok) break;
         uint8_t* unit = sm + Q_RING + slot * QUNIT;
@@ -402,7 +442,7 @@ __device__ void scorer(const VerifyArgs& a, const PoolMaps& maps, const Item& it
     }
     asm volatile("cp.async.wait_all;" ::: "memory");
   } else if (warp == 13 && lane == 0) {
-    tma_issuer(a, it, c, 3, QSLOTS, [&](int n, int t, int u, int slot, uint64_t* bar) {
+    tma_issuer(a, it, c, 3, QSLOTS, &c->q_ready, [&](int n, int t, int u, int slot, uint64_t* bar) {
       (void)n;
       uint8_t* unit = sm + Q_RING + slot * QUNIT;
       const bool load = c->icontig[t % NIDX] != 0;
@@ -418,16 +458,22 @@ __device__ void scorer(const VerifyArgs& a, const PoolMaps& maps, const Item& it
       // ---- MMA issuer for the pair: one tile at a time, once all of it landed
       constexpr uint32_t idesc = idesc_bf16_f32(256, 128, false, false);
       const uint64_t rope_desc = desc_sw128(smem_u32(sm + Q_ROPE), 16, 1024);
-      bool ok = wait_clu(&c->q_ready, 0, c, a.status);
+      join_cluster(joined);
+      bool ok = wait_bar(&c->q_ready, 0, c, a.status);
       tc_fence_after();
       for (int t = 0; t < it.ntiles && ok; ++t) {
         const int s = t & 1;
         const uint32_t sbuf = tmem + 256 + 128 * s;
-        ok = wait_clu(&c->sempty[s], ((t >> 1) & 1) ^ 1, c, a.status);
-        for (int u = 0; u < 3 && ok; ++u) {
-          const int n = 3 * t + u, slot = n % QSLOTS;
+        ok = wait_bar(&c->sempty[s], ((t >> 1) & 1) ^ 1, c, a.status);
+        // Only the tile's last unit is waited for, here and in the peer: each
+        // producer counts itself in on a unit only after its share of every
+        // earlier unit landed (cp.async arrivals fire once all of the lane's
+        // earlier copies completed; the TMA forwarder and the follower's
+        // forwards go unit by unit in order).
+        {
+          const int n = 3 * t + 2, slot = n % QSLOTS;
           const uint32_t ph = (n / QSLOTS) & 1;
-          ok = wait_cta(&c->full[slot], ph, c, a.status) && wait_clu(&c->peer[slot], ph, c, a.status);
+          ok = ok && wait_bar(&c->full[slot], ph, c, a.status) && wait_bar(&c->peer[slot], ph, c, a.status);
         }
         if (!ok) break;
         fence_async_smem();  // cp.async (generic proxy) data -> tensor-core reads
@@ -451,12 +497,13 @@ __device__ void scorer(const VerifyArgs& a, const PoolMaps& maps, const Item& it
     } else {
       // ---- follower: forward "my unit n is full" to the leader
       const uint32_t lead_peer = map_cluster(smem_u32(&c->peer[0]), rank - 1);
+      join_cluster(joined);
       // The leader's MMAs read this CTA's Q too: it must be in place before
       // the first forward.
-      if (!wait_clu(&c->q_ready, 0, c, a.status)) return;
+      if (!wait_bar(&c->q_ready, 0, c, a.status)) return;
       for (int n = 0; n < 3 * it.ntiles; ++n) {
         const int slot = n % QSLOTS;
-        if (!wait_cta(&c->full[slot], (n / QSLOTS) & 1, c, a.status)) return;
+        if (!wait_bar(&c->full[slot], (n / QSLOTS) & 1, c, a.status)) return;
         fence_async_smem();
         signal_remote(lead_peer + slot * 8);
       }
@@ -470,39 +517,39 @@ __device__ void scorer(const VerifyArgs& a, const PoolMaps& maps, const Item& it
     const bool row_ok = req_row < a.rows_per_req;
     const uint32_t lane_addr = tmem + ((uint32_t)(w * 32) << 16);
     {
-      // Q into place while the producers already gather: this half's 256
-      // latent values -> TMEM lane r, this half's 32 rope values -> smem.
-      const size_t g = (size_t)it.loc.b * a.rows_per_req + (row_ok ? req_row : 0);
-      const uint4* ql = reinterpret_cast<const uint4*>(a.q_latent + g * a.q_lat_stride) + 32 * hw;
+      // Parents of the request's nodes, for the ancestor bits below.
+      const int T = a.n_nodes;
+      const bool owns_node = hw == 0 && r < T;
+      const int par_r = owns_node ? __ldg(a.tree_parent + (size_t)it.loc.b * T + r) : 0;
+      // Q latent of row r, this half's 256 values: the TMA staging (eight
+      // 128-byte-swizzled 64-column boxes) -> TMEM lane r.  Q rope came by
+      // TMA straight into its place.
+      if (wait_bar(&c->qload, 0, c, a.status)) {
+        const uint8_t* row = sm + Q_LAT_STAGE + r * 128;
 #pragma unroll 1
-      for (int b4 = 0; b4 < 2; ++b4) {
-        uint4 x[16];
+        for (int b4 = 0; b4 < 4; ++b4) {
+          const uint8_t* box = row + (4 * hw + b4) * (ROWS * 128);
+          uint32_t v[2][16];
 #pragma unroll
-        for (int e = 0; e < 16; ++e) x[e] = row_ok ? __ldg(ql + 16 * b4 + e) : make_uint4(0, 0, 0, 0);
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          uint32_t v[16];
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            v[4 * e] = x[4 * q + e].x; v[4 * e + 1] = x[4 * q + e].y;
-            v[4 * e + 2] = x[4 * q + e].z; v[4 * e + 3] = x[4 * q + e].w;
+          for (int j = 0; j < 8; ++j) {  // 16-byte piece j: latent columns 8j .. 8j+7 of the box
+            const uint4 x = *reinterpret_cast<const uint4*>(box + ((j ^ (r & 7)) << 4));
+            uint32_t* d = &v[j >> 2][4 * (j & 3)];
+            d[0] = x.x; d[1] = x.y; d[2] = x.z; d[3] = x.w;
           }
-          tmem_st16(lane_addr + 128 * hw + 64 * b4 + 16 * q, v);
+          tmem_st16(lane_addr + 128 * hw + 32 * b4, v[0]);
+          tmem_st16(lane_addr + 128 * hw + 32 * b4 + 16, v[1]);
         }
       }
-      const uint4* qr = reinterpret_cast<const uint4*>(a.q_rope + g * a.q_rope_stride) + 4 * hw;
-      uint4 y[4];
-#pragma unroll
-      for (int c16 = 0; c16 < 4; ++c16) y[c16] = row_ok ? __ldg(qr + c16) : make_uint4(0, 0, 0, 0);
-#pragma unroll
-      for (int c16 = 0; c16 < 4; ++c16)
-        *reinterpret_cast<uint4*>(sm + Q_ROPE + r * 128 + (((4 * hw + c16) ^ (r & 7)) << 4)) = y[c16];
       tmem_st_wait();
-      fence_async_smem();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&c->q_ready);
+      if (lane == 0) mbar_arrive(&c->q_ready);  // also: the staging is free for keys
+      if (owns_node) c->par[r] = par_r;
+      named_bar(1, 256);
+      if (owns_node) c->anc[r] = ancestor_bits_smem(c->par, r, T, a.status);
+      named_bar(1, 256);
     }
+    join_cluster(joined);  // remote from here on: sempty arrives, P copies
     const uint64_t anc = row_ok ? c->anc[req_row / a.n_heads] : 0ull;
     const float scale2 = a.sm_scale * 1.4426950408889634f;  // scores in log2 units
     float m_ref = -INFINITY, l = 0.f;
@@ -521,7 +568,7 @@ __device__ void scorer(const VerifyArgs& a, const PoolMaps& maps, const Item& it
         for (int q = 0; q < 2; ++q) km[q] = __ballot_sync(0xffffffffu, keys[32 * q + lane] >= 0);
         release_ring(c, t, lane);
       }
-      wait_clu(&c->sfull[s], (t >> 1) & 1, c, a.status);  // on expiry: continue, stop below
+      wait_bar(&c->sfull[s], (t >> 1) & 1, c, a.status);  // on expiry: continue, stop below
       tc_fence_after();
       uint32_t xr[2][32];  // raw fp32 scores of this row, this half's 64 keys
 #pragma unroll
@@ -596,7 +643,7 @@ __device__ void scorer(const VerifyArgs& a, const PoolMaps& maps, const Item& it
       named_bar(1, 256);
       if (r == 0 && hw == 0 && !aborted(c)) {
         // The accumulator's P buffer s is free once it finished tile t-2.
-        if (wait_clu(&c->pfree[s], ((t >> 1) & 1) ^ 1, c, a.status)) {
+        if (wait_bar(&c->pfree[s], ((t >> 1) & 1) ^ 1, c, a.status)) {
           asm volatile(
               "cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];\n"
               "cp.async.bulk.commit_group;" ::"r"(peer_pbuf + s * PBUF),
@@ -619,7 +666,7 @@ __device__ void scorer(const VerifyArgs& a, const PoolMaps& maps, const Item& it
 
 // ------------------------------------------------------------ accumulator
 __device__ void accumulator(const VerifyArgs& a, const PoolMaps& maps, const Item& it, uint8_t* sm, Ctrl* c,
-                            uint32_t rank) {
+                            uint32_t rank, bool& joined) {
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const uint32_t tmem = c->tmem_base;  // O: cols [0,512)
   const bool leader = (rank & 1) == 0;
@@ -643,7 +690,7 @@ __device__ void accumulator(const VerifyArgs& a, const PoolMaps& maps, const Ite
       for (int j = 0; j < G; ++j) ids[j] = keys[4 * (G * lsu + j) + (lane >> 3)];
       release_ring(c, t, lane);
       bool ok = true;
-      if (lane == 0) ok = wait_clu(&c->empty[s], ((t >> 1) & 1) ^ 1, c, a.status);
+      if (lane == 0) ok = wait_bar(&c->empty[s], ((t >> 1) & 1) ^ 1, c, a.status);
       if (!__shfl_sync(0xffffffffu, ok, 0)) break;
       uint8_t* slot = sm + V_RING + s * VSLOT;
       if (!contig) {
@@ -654,7 +701,7 @@ __device__ void accumulator(const VerifyArgs& a, const PoolMaps& maps, const Ite
     }
     asm volatile("cp.async.wait_all;" ::: "memory");
   } else if (warp == 10 && lane == 0) {
-    tma_issuer(a, it, c, 1, VSLOTS, [&](int n, int t, int u, int slot, uint64_t* bar) {
+    tma_issuer(a, it, c, 1, VSLOTS, nullptr, [&](int n, int t, int u, int slot, uint64_t* bar) {
       (void)n;
       (void)u;
       uint8_t* dst = sm + V_RING + slot * VSLOT;
@@ -669,12 +716,12 @@ __device__ void accumulator(const VerifyArgs& a, const PoolMaps& maps, const Ite
     if (leader) {
       // ---- MMA issuer for the pair: O[rows, 128q .. 128q+127] += P V
       constexpr uint32_t idesc = idesc_bf16_f32(256, 128, false, true);  // A = P K-major, B = V MN-major
+      join_cluster(joined);
       for (int t = 0; t < it.ntiles; ++t) {
         const int s = t & 1;
         const uint32_t ph = (t >> 1) & 1;
-        if (!wait_clu(&c->pfull[s], ph, c, a.status) || !wait_clu(&c->ppeer[s], ph, c, a.status) ||
-            !wait_clu(&c->corr_done[s], ph, c, a.status) || !wait_cta(&c->full[s], ph, c, a.status) ||
-            !wait_clu(&c->peer[s], ph, c, a.status))
+        if (!wait_bar(&c->pfull[s], ph, c, a.status) || !wait_bar(&c->full[s], ph, c, a.status) ||
+            !wait_bar(&c->peer[s], ph, c, a.status) || !wait_bar(&c->corr_done[s], ph, c, a.status))
           break;
         fence_async_smem();  // cp.async (generic proxy) data -> tensor-core reads
         tc_fence_after();
@@ -693,15 +740,14 @@ __device__ void accumulator(const VerifyArgs& a, const PoolMaps& maps, const Ite
       }
       commit2(&c->mma_done, kAccPair);
     } else {
-      // ---- follower: forward "my P tile / my slot of tile t is full" to the leader
-      const uint32_t lead_ppeer = map_cluster(smem_u32(&c->ppeer[0]), rank - 1);
+      // ---- follower: forward "my P tile and my value slot of tile t are
+      // both full" to the leader, as one arrive
       const uint32_t lead_peer = map_cluster(smem_u32(&c->peer[0]), rank - 1);
+      join_cluster(joined);
       for (int t = 0; t < it.ntiles; ++t) {
         const int s = t & 1;
         const uint32_t ph = (t >> 1) & 1;
-        if (!wait_clu(&c->pfull[s], ph, c, a.status)) return;
-        signal_remote(lead_ppeer + s * 8);
-        if (!wait_cta(&c->full[s], ph, c, a.status)) return;
+        if (!wait_bar(&c->pfull[s], ph, c, a.status) || !wait_bar(&c->full[s], ph, c, a.status)) return;
         fence_async_smem();
         signal_remote(lead_peer + s * 8);
       }
@@ -709,10 +755,11 @@ __device__ void accumulator(const VerifyArgs& a, const PoolMaps& maps, const Ite
   } else if (warp == 2 && lane == 0) {
     // ---- relay: PV of tile t finished -> re-arm P buffer s, release it to the scorer
     const uint32_t sc_pfree = map_cluster(smem_u32(&c->pfree[0]), scorer_rank);
+    join_cluster(joined);
     for (int s = 0; s < 2; ++s) mbar_arrive_expect_tx(&c->pfull[s], PCOPY);
     for (int t = 0; t < it.ntiles; ++t) {
       const int s = t & 1;
-      if (!wait_clu(&c->pvdone[s], (t >> 1) & 1, c, a.status)) break;
+      if (!wait_bar(&c->pvdone[s], (t >> 1) & 1, c, a.status)) break;
       if (t + 2 < it.ntiles) mbar_arrive_expect_tx(&c->pfull[s], PCOPY);
       signal_remote(sc_pfree + s * 8);
     }
@@ -723,10 +770,11 @@ __device__ void accumulator(const VerifyArgs& a, const PoolMaps& maps, const Ite
     const uint32_t lane_addr = tmem + ((uint32_t)(w * 32) << 16);
     const uint32_t sc_pfree = map_cluster(smem_u32(&c->pfree[0]), scorer_rank);
     const uint32_t lead_corr = map_cluster(smem_u32(&c->corr_done[0]), rank & ~1u);
+    join_cluster(joined);
     float lfin = 0.f;
     for (int t = 0; t < it.ntiles; ++t) {
       const int s = t & 1;
-      wait_clu(&c->pfull[s], (t >> 1) & 1, c, a.status);  // on expiry: continue, stop below
+      wait_bar(&c->pfull[s], (t >> 1) & 1, c, a.status);  // on expiry: continue, stop below
       const uint8_t* pb = sm + V_PBUF + s * PBUF;
       const float* meta = reinterpret_cast<const float*>(pb + PTILE);
       const uint32_t* flags = reinterpret_cast<const uint32_t*>(meta + 384);
@@ -734,7 +782,7 @@ __device__ void accumulator(const VerifyArgs& a, const PoolMaps& maps, const Ite
       if (flags[0] | flags[1] | flags[2] | flags[3]) {
         const float alpha = meta[r];
         // O must hold PV of tiles < t before it is rescaled.
-        wait_clu(&c->pvdone[(t - 1) & 1], ((t - 1) >> 1) & 1, c, a.status);
+        wait_bar(&c->pvdone[(t - 1) & 1], ((t - 1) >> 1) & 1, c, a.status);
         tc_fence_after();
         if (__any_sync(0xffffffffu, alpha != 1.f)) {  // warp-collective TMEM access
           uint32_t v[16];
@@ -762,7 +810,7 @@ __device__ void accumulator(const VerifyArgs& a, const PoolMaps& maps, const Ite
     // shared-memory box (4 rotating 16 KB boxes in the free value ring) ->
     // one TMA store, which writes whole rows' slices coalesced and clips
     // the rows past the request.
-    const bool done = wait_clu(&c->mma_done, 0, c, a.status);
+    const bool done = wait_bar(&c->mma_done, 0, c, a.status);
     tc_fence_after();
     const int req_row = it.row0 + r;
     const bool row_ok = req_row < a.rows_per_req;
@@ -837,7 +885,7 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(kThreads, 1)
   // All four CTAs see the same key range; an empty item skips all work but
   // still takes part in the cluster barriers and the pair's TMEM allocation.
 
-  if (rank < 2 && have && tid < a.n_nodes) c->par[tid] = __ldg(a.tree_parent + (size_t)it.loc.b * a.n_nodes + tid);
+  const bool work = have && it.ntiles > 0;
   if (tid == 0) {
     for (int i = 0; i < kMaxSlots; ++i) {
       mbar_init(&c->full[i], 32 * kLsuWarps + 1);  // every load/store-unit lane, the TMA forwarder
@@ -851,7 +899,6 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(kThreads, 1)
       mbar_init(&c->sempty[i], 16);
       mbar_init(&c->pfree[i], 2);
       mbar_init(&c->pfull[i], 1);
-      mbar_init(&c->ppeer[i], 1);
       mbar_init(&c->pvdone[i], 1);
       mbar_init(&c->corr_done[i], 8);
     }
@@ -863,9 +910,17 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(kThreads, 1)
     }
     mbar_init(&c->mma_done, 1);
     mbar_init(&c->q_ready, 8);
+    mbar_init(&c->qload, 1);
     c->abort = 0;
     c->wait_ns = a.wait_ns;
     fence_mbar_init();
+    if (rank < 2 && work) {
+      // The scorer's Q first: latent into the staging, rope into place.
+      const int g0 = it.loc.b * a.rows_per_req + it.row0;
+      mbar_arrive_expect_tx(&c->qload, Q_LAT_BYTES + Q_ROPE_BYTES);
+      for (int b = 0; b < kLatent / 64; ++b) tma_run(&maps.ql, sm + Q_LAT_STAGE + b * (ROWS * 128), b, g0, &c->qload);
+      tma_run(&maps.qr, sm + Q_ROPE, 0, g0, &c->qload);
+    }
   }
   if (warp == 3) {
     asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(&c->tmem_base)),
@@ -873,26 +928,26 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(kThreads, 1)
                  : "memory");
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
   }
-  __syncthreads();
-  if (rank < 2 && have) {
-    const int T = a.n_nodes;
-    if (tid < T) c->anc[tid] = ancestor_bits_smem(c->par, tid, T, a.status);
-  }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
 
-  cluster_sync();  // all four CTAs' barriers and TMEM ready before any remote traffic
-
-  if (have && it.ntiles > 0) {
-    if (rank < 2) scorer(a, maps, it, sm, c, rank);
-    else accumulator(a, maps, it, sm, c, rank);
+  // This CTA's barriers and TMEM are ready for the others; each thread waits
+  // for theirs before its first remote action (join_cluster).
+  asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+  bool joined = false;
+  if (work) {
+    if (rank < 2) scorer(a, maps, it, sm, c, rank, joined);
+    else accumulator(a, maps, it, sm, c, rank, joined);
   }
+  join_cluster(joined);
+  // The Q loads have landed before the CTA leaves (also after an expired wait).
+  if (tid == 0 && rank < 2 && work) mbar_wait(&c->qload, 0, kDrainNs);
 
   tc_fence_before();
   __syncthreads();
   // Tensor-core work writing this CTA's TMEM must be finished before it is freed.
-  if (warp == 3 && have && it.ntiles > 0) mbar_wait_cluster(&c->mma_done, 0, global_timer_ns() + kDrainNs);
+  if (warp == 3 && work) mbar_wait_cluster(&c->mma_done, 0, kDrainNs);
   tc_fence_before();
   __syncthreads();
   cluster_sync();  // no remote copy or arrival may target a CTA that has exited
@@ -908,13 +963,15 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(kThreads, 1)
     if (tid == 0) {
       __threadfence();
       atomicAdd(a.grid_done, 1u);
-      const uint64_t deadline = global_timer_ns() + a.wait_ns;
+      uint64_t deadline = 0;
       bool ok = true;
-      for (uint32_t spin = 0;; ++spin) {
+      for (uint32_t spin = 1;; ++spin) {
         uint32_t v;
         asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(a.grid_done) : "memory");
         if (v >= gridDim.x) break;
-        if ((spin & 63u) == 63u && global_timer_ns() > deadline) {
+        if (spin == 4u) {
+          deadline = global_timer_ns() + a.wait_ns;
+        } else if ((spin & 63u) == 0u && global_timer_ns() > deadline) {
           ok = false;
           break;
         }
@@ -979,6 +1036,20 @@ cudaError_t make_pool_maps(const VerifyArgs& a, PoolMaps* m) {
   const cuuint32_t obox[3] = {64, (cuuint32_t)ROWS, 1}, oes[3] = {1, 1, 1};
   if (enc(&m->po, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, a.partial_o, odims, ostrides, obox, oes,
           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+    return cudaErrorInvalidValue;
+  // Queries: rows (t, h) of all requests, request-major; rows past the last
+  // one read as zeros.  The row strides are multiples of 8 elements and the
+  // bases 16-byte aligned (checked when the call is validated).
+  const cuuint64_t qrows = (cuuint64_t)a.batch * (cuuint64_t)a.rows_per_req;
+  const cuuint64_t qldims[2] = {(cuuint64_t)kLatent, qrows}, qlstr[1] = {(cuuint64_t)a.q_lat_stride * 2};
+  const cuuint64_t qrdims[2] = {(cuuint64_t)kRope, qrows}, qrstr[1] = {(cuuint64_t)a.q_rope_stride * 2};
+  const cuuint32_t qbox[2] = {64, (cuuint32_t)ROWS};
+  if (enc(&m->ql, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<uint16_t*>(a.q_latent), qldims, qlstr, qbox,
+          es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS ||
+      enc(&m->qr, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<uint16_t*>(a.q_rope), qrdims, qrstr, qbox,
+          es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
     return cudaErrorInvalidValue;
   return cudaSuccess;

@@ -65,18 +65,27 @@ __device__ __forceinline__ bool mbar_try_wait_cluster(uint64_t* bar, uint32_t pa
       : "memory");
   return ok != 0;
 }
-// Bounded wait on a phase: false once `deadline_ns` (global timer) passes.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint64_t deadline_ns) {
-  for (uint32_t it = 0;; ++it) {
-    if (mbar_try_wait(bar, parity)) return true;
-    if ((it & 63u) == 63u && global_timer_ns() > deadline_ns) return false;
+// Bounded wait on a phase: false once about `limit_ns` (global timer) have
+// passed.  The timer is first read after four unsuccessful tries, then every
+// 64: a timer read costs far more than a try, and most waits here find the
+// phase already complete.
+template <bool kCluster>
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity, uint64_t limit_ns) {
+  uint64_t deadline = 0;
+  for (uint32_t it = 1;; ++it) {
+    if (kCluster ? mbar_try_wait_cluster(bar, parity) : mbar_try_wait(bar, parity)) return true;
+    if (it == 4u) {
+      deadline = global_timer_ns() + limit_ns;
+    } else if ((it & 63u) == 0u && global_timer_ns() > deadline) {
+      return false;
+    }
   }
 }
-__device__ __forceinline__ bool mbar_wait_cluster(uint64_t* bar, uint32_t parity, uint64_t deadline_ns) {
-  for (uint32_t it = 0;; ++it) {
-    if (mbar_try_wait_cluster(bar, parity)) return true;
-    if ((it & 63u) == 63u && global_timer_ns() > deadline_ns) return false;
-  }
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint64_t limit_ns) {
+  return mbar_wait_bounded<false>(bar, parity, limit_ns);
+}
+__device__ __forceinline__ bool mbar_wait_cluster(uint64_t* bar, uint32_t parity, uint64_t limit_ns) {
+  return mbar_wait_bounded<true>(bar, parity, limit_ns);
 }
 
 // ---------------------------------------------------------------- TMEM
