@@ -414,6 +414,7 @@ def run_ours(args, world, rank, local):
     if rank != 0:
         return
     flops, byts = cost["flops"], cost["bytes"]
+    fused = bool(dv.plan.fused_combine)
     tc_peak = peaks["bf16_tflops"]
     achieved = flops / (partial_us * 1e-6) / 1e12
     roof_us = max(byts / (peaks["hbm_gbs"] * 1e9), flops / (tc_peak * 1e12)) * 1e6
@@ -432,20 +433,25 @@ def run_ours(args, world, rank, local):
         "gbs": byts / (call_us * 1e-6) / 1e9,
         "tflops": flops / (call_us * 1e-6) / 1e12,
         "roofline_us": roof_us, "roofline_frac_call": roof_us / call_us,
-        "partial_kernel_us": partial_us, "combine_kernel_us": statistics.mean(combines),
+        "partial_kernel_us": partial_us,
+        # With the merge in the partial kernel there is no combine launch (the
+        # event pair around the absent launch only measures event overhead).
+        "combine_kernel_us": None if fused else statistics.mean(combines),
+        "merge": "in the partial kernel (cooperative launch)" if fused else "combine_kernel",
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": tc_peak, "unit": "TFLOP/s",
                      "frac": achieved / tc_peak,
                      "traffic": _traffic({1: "k_partial_simt.cu", 2: "k_partial_tc.cu",
                                           3: "k_partial_tc2.cu"}[dv.plan.kernel])
                      if args.workload == "long_scattered" else None,
                      "peak_source": peaks["source"] + " bf16 burst (MEASURED_PEAKS.json)",
-                     "kernel": "split-KV partial (%s)" % {1: "simt", 2: "tcgen05 pair", 3: "tcgen05 cta_group::2 quad"}[dv.plan.kernel]},
+                     "kernel": "split-KV partial (%s)%s" % ({1: "simt", 2: "tcgen05 pair", 3: "tcgen05 cta_group::2 quad"}[dv.plan.kernel],
+                                                            " incl. the split merge" if fused else "")},
         "alg_bytes": byts, "alg_flops": flops,
         "plan": dv.plan.as_dict(),
         "contiguous_us": contiguous_us,
         "scatter_over_contiguous": (call_us / contiguous_us) if contiguous_us else None,
         "cpu_baseline": cpu, "e2e": e2e, "clocks": clocks,
-        "gpu_launches": 2 * args.steps,
+        "gpu_launches": (1 if fused else 2) * args.steps,
         "status_word": status, "wall_s_timed_region": wall,
     }
     print(json.dumps(line), flush=True)

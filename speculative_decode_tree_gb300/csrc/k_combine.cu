@@ -15,7 +15,10 @@ constexpr int kCombineWarps = 8;
 
 __global__ void __launch_bounds__(32 * kCombineWarps) combine_kernel(const VerifyArgs a) {
   const int u = blockIdx.x * kCombineWarps + (threadIdx.x >> 5);
-  if (u < combine_units(a)) combine_unit(a, u, threadIdx.x & 31, false);
+  if (u >= combine_units(a)) return;
+  int first, count;
+  combine_slots(a, u, threadIdx.x & 31, first, count);
+  combine_unit(a, u, threadIdx.x & 31, first, count);
 }
 
 __global__ void ancestor_mask_kernel(const int32_t* parent, int T, uint64_t* anc, uint32_t* status) {

@@ -960,6 +960,13 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(kThreads, 1)
     // once (cooperative launch), so each counts itself done and waits,
     // bounded, for all others; then the warps of the grid share the
     // (row, 64-column) merge units.  A timed-out wait anywhere writes zeros.
+    // Each warp looks up its first unit's split range while the grid
+    // finishes.
+    const int units = combine_units(a);
+    const int stride = gridDim.x * (kThreads / 32);
+    int u = blockIdx.x * (kThreads / 32) + warp;
+    int first = 0, count = 0;
+    if (u < units) combine_slots(a, u, tid & 31, first, count);
     if (tid == 0) {
       __threadfence();
       atomicAdd(a.grid_done, 1u);
@@ -983,9 +990,10 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(kThreads, 1)
     }
     __syncthreads();
     const bool zero = c->merge_zero != 0;
-    const int units = combine_units(a);
-    for (int u = blockIdx.x * (kThreads / 32) + warp; u < units; u += gridDim.x * (kThreads / 32))
-      combine_unit(a, u, tid & 31, zero);
+    for (; u < units; u += stride) {
+      combine_unit(a, u, tid & 31, first, zero ? 0 : count);
+      if (u + stride < units) combine_slots(a, u + stride, tid & 31, first, count);
+    }
   }
 }
 
