@@ -99,18 +99,18 @@ static_assert(Q_LAT_STAGE % 1024 == 0, "128-byte swizzle wants 1024-byte aligned
 constexpr int V_PBUF = 0;                               // accumulator: 2 x PBUF
 constexpr int V_RING = V_PBUF + 2 * PBUF;               // accumulator: 2 x 64 KB
 constexpr int V_END = V_RING + VSLOTS * VSLOT;
+static_assert(VSLOTS * VSLOT >= 8 * ROWS * 128, "the epilogue's eight 16 KB boxes fit the value ring");
 constexpr int IDX_RING = (Q_END > V_END ? Q_END : V_END);  // both: NIDX x 128 int32
 constexpr int BIG_END = IDX_RING + NIDX * TK * 4;
 
 
 struct __align__(8) Ctrl {
   // Ring slot barriers (per unit slot): full = this CTA's chunks of the unit
-  // landed (every load/store-unit lane + the TMA forwarder), peer = (leader)
+  // landed (every load/store-unit lane + the TMA stream), peer = (leader)
   // the follower's slot is full, empty = the pair's MMAs consumed the slot
   // (commit multicast to both CTAs of the pair); tma = the TMA stream's
   // loads of the unit landed.
   uint64_t full[kMaxSlots], peer[kMaxSlots], empty[kMaxSlots], tma[kMaxSlots];
-  uint32_t tma_issued;  // units whose TMA loads the issuer has started (bit 31: done)
   // scorer
   uint64_t sfull[2], sempty[2], pfree[2];
   // accumulator
@@ -343,59 +343,50 @@ __device__ __forceinline__ void tma_run(const CUtensorMap* map, uint8_t* dst, in
       : "memory");
 }
 
-// The TMA stream of a CTA over a ring of `nslots` unit slots, `upt` units
-// per tile, run by two warps (lane 0 of each).  The issuer starts each unit's
-// loads once its slot is free: `issue(n, t, u, slot, bar)` arms the stream's
-// barrier `bar` with the unit's bytes -- possibly none -- and starts them.  The
-// forwarder waits for each issued unit's bytes and then counts the stream in
-// on the slot's full barrier.  A non-null `gate2` is waited for (phase 0)
-// before unit 2 is issued.  They are separate warps because a lane
-// suspended in a barrier wait holds back the other lanes of its warp: an
-// issuer waiting for a slot that only frees once a landed unit is forwarded
-// would stall its own forwarder.  After an expired wait the forwarder still
-// waits (fixed bound) for every unit the issuer started, so no load is in
-// flight when the CTA leaves.
+// The TMA stream of a CTA: 2-D tile loads of the units of contiguous tiles,
+// over a ring of `nslots` unit slots, `upt` units per tile.  One thread
+// issues: it starts each such unit's loads once the slot is free,
+// `issue(n, t, u, slot, bar)` arming the slot's barrier `bar` with the bytes.
+// Lane 0 of load/store-unit warp 0 counts the stream in on the slot's full
+// barrier: at once for a scattered unit (no TMA bytes), once the bytes landed
+// for a contiguous one.  Both sides track the phase parity of each slot's
+// TMA barrier from the same per-tile flags.  A non-null `gate2` is waited for
+// (phase 0) before unit 2 is loaded.  Only the last load started on a slot
+// can still be in flight (an earlier one was consumed before its slot was
+// reused), so before it leaves the issuer waits (fixed bound) for those.
 template <typename Issue>
 __device__ __forceinline__ void tma_issuer(const VerifyArgs& a, const Item& it, Ctrl* c, int upt, int nslots,
                                            uint64_t* gate2, Issue&& issue) {
-  volatile uint32_t* issued = &c->tma_issued;
+  uint32_t par = 0, armed = 0;  // per slot: parity of the next TMA phase; a load was started
   const int nunits = it.ntiles * upt;
   for (int n = 0; n < nunits; ++n) {
     const int t = n / upt, u = n - t * upt, slot = n % nslots;
     if (u == 0 && !wait_ring(a, c, t)) break;
-    const bool free = (n != 2 || gate2 == nullptr || wait_bar(gate2, 0, c, a.status)) &&
-                      wait_bar(&c->empty[slot], ((n / nslots) & 1) ^ 1, c, a.status);
-    if (free) issue(n, t, u, slot, &c->tma[slot]);
-    if (!free || u == upt - 1) mbar_arrive(&c->iempty[t % NIDX]);
-    if (!free) break;
-    __threadfence_block();
-    *issued = (uint32_t)(n + 1);
-  }
-  __threadfence_block();
-  *issued = *issued | 0x80000000u;  // done issuing
-}
-__device__ __forceinline__ void tma_forwarder(const VerifyArgs& a, const Item& it, Ctrl* c, int upt, int nslots) {
-  volatile uint32_t* issued = &c->tma_issued;
-  const int nunits = it.ntiles * upt;
-  for (int n = 0; n < nunits; ++n) {
-    // Wait (bounded) until the issuer started unit n or stopped.
-    uint32_t v = *issued;
-    if ((v & 0x7fffffffu) <= (uint32_t)n && !(v & 0x80000000u)) {
-      const uint64_t deadline = global_timer_ns() + kDrainNs;
-      while ((v & 0x7fffffffu) <= (uint32_t)n && !(v & 0x80000000u) && global_timer_ns() < deadline) {
-        __nanosleep(32);
-        v = *issued;
+    bool free = true;
+    if (c->icontig[t % NIDX] != 0) {
+      free = (n != 2 || gate2 == nullptr || wait_bar(gate2, 0, c, a.status)) &&
+             wait_bar(&c->empty[slot], ((n / nslots) & 1) ^ 1, c, a.status);
+      if (free) {
+        issue(n, t, u, slot, &c->tma[slot]);
+        par ^= 1u << slot;
+        armed |= 1u << slot;
       }
     }
-    if ((v & 0x7fffffffu) <= (uint32_t)n) break;  // never issued
-    const int slot = n % nslots;
-    if (!mbar_wait(&c->tma[slot], (n / nslots) & 1, kDrainNs)) {
-      atomicOr(a.status, DDTREE_ST_TIMEOUT);
-      c->abort = 1;
-      break;
-    }
-    mbar_arrive(&c->full[slot]);
+    if (!free || u == upt - 1) mbar_arrive(&c->iempty[t % NIDX]);
+    if (!free) break;
   }
+  for (int slot = 0; slot < nslots; ++slot)
+    if ((armed >> slot) & 1u) mbar_wait(&c->tma[slot], ((par >> slot) & 1u) ^ 1u, kDrainNs);
+}
+// Lane 0 of load/store-unit warp 0: count the TMA stream in on unit slot
+// `slot` (see tma_issuer); `tpar` is this side's copy of the parities.
+__device__ __forceinline__ bool tma_count_in(const VerifyArgs& a, Ctrl* c, bool contig, int slot, uint32_t& tpar) {
+  if (contig) {
+    if (!wait_bar(&c->tma[slot], (tpar >> slot) & 1u, c, a.status)) return false;
+    tpar ^= 1u << slot;
+  }
+  mbar_arrive(&c->full[slot]);
+  return true;
 }
 
 // ------------------------------------------------------------------ scorer
@@ -406,13 +397,14 @@ __device__ void scorer(const VerifyArgs& a, const PoolMaps& maps, const Item& it
   const bool leader = (rank & 1) == 0;
   const int half = rank & 1;           // which 64 keys of each tile this CTA gathers
 
-  // Producer warps: load/store unit {0, 2, 3, 12}; TMA issuer 13 and
-  // forwarder 14 (contiguous runs).
+  // Producer warps: load/store unit {0, 2, 3, 12}; TMA issuer 13
+  // (contiguous runs).  MMA issuers (leader): 1 (even tiles), 14 (odd).
   const int lsu = warp == 0 ? 0 : warp == 2 ? 1 : warp == 3 ? 2 : warp == 12 ? 3 : -1;
   if (warp == kLoaderWarp) {
     index_loader(a, it, sm, c);
   } else if (lsu >= 0) {
     constexpr int G = 16 / kLsuWarps;  // groups of four keys per warp (of the half's 16)
+    uint32_t tpar = 0;                 // (warp 0) TMA phase parities, see tma_issuer
     for (int t = 0; t < it.ntiles; ++t) {
       if (!wait_ring(a, c, t)) break;
       const int* keys = ring_tile(sm, t) + HALF * half;
@@ -437,6 +429,10 @@ __device__ void scorer(const VerifyArgs& a, const PoolMaps& maps, const Item& it
           for (int cc = 0; cc < 3; ++cc) lsu_chunk<G>(a.kv_pool, unit + cc * SCHUNK, 3 * u + cc, 4 * G * lsu, ids, lane);
         }
         cp_async_mbar_arrive(&c->full[slot]);
+        if (lsu == 0) {
+          if (lane == 0) ok = tma_count_in(a, c, contig, slot, tpar);
+          ok = __shfl_sync(0xffffffffu, ok, 0);
+        }
       }
       if (!ok) break;
     }
@@ -451,25 +447,25 @@ __device__ void scorer(const VerifyArgs& a, const PoolMaps& maps, const Item& it
         for (int cc = 0; cc < 3; ++cc)
           tma_run(&maps.half, unit + cc * SCHUNK, 3 * u + cc, c->ifirst[t % NIDX] + HALF * half, bar);
     });
-  } else if (warp == 14 && lane == 0) {
-    tma_forwarder(a, it, c, 3, QSLOTS);
-  } else if (warp == 1 && lane == 0) {
-    if (leader) {
-      // ---- MMA issuer for the pair: one tile at a time, once all of it landed
+  } else if (leader && (warp == 1 || warp == 14) && lane == 0) {
+    // ---- MMA issuers for the pair, one per S buffer: warp 1 takes the even
+    // tiles, warp 14 the odd ones, so one issuer's waits for its next tile
+    // overlap the other's MMAs.  Each tile once all of it landed.
+    {
       constexpr uint32_t idesc = idesc_bf16_f32(256, 128, false, false);
       const uint64_t rope_desc = desc_sw128(smem_u32(sm + Q_ROPE), 16, 1024);
+      const int s = warp == 1 ? 0 : 1;
       join_cluster(joined);
       bool ok = wait_bar(&c->q_ready, 0, c, a.status);
       tc_fence_after();
-      for (int t = 0; t < it.ntiles && ok; ++t) {
-        const int s = t & 1;
+      for (int t = s; t < it.ntiles && ok; t += 2) {
         const uint32_t sbuf = tmem + 256 + 128 * s;
         ok = wait_bar(&c->sempty[s], ((t >> 1) & 1) ^ 1, c, a.status);
         // Only the tile's last unit is waited for, here and in the peer: each
         // producer counts itself in on a unit only after its share of every
         // earlier unit landed (cp.async arrivals fire once all of the lane's
-        // earlier copies completed; the TMA forwarder and the follower's
-        // forwards go unit by unit in order).
+        // earlier copies completed; the TMA stream's count and the
+        // follower's forwards go unit by unit in order).
         {
           const int n = 3 * t + 2, slot = n % QSLOTS;
           const uint32_t ph = (n / QSLOTS) & 1;
@@ -494,7 +490,9 @@ __device__ void scorer(const VerifyArgs& a, const PoolMaps& maps, const Item& it
         commit2(&c->sfull[s], kScorerPair);
       }
       commit2(&c->mma_done, kScorerPair);
-    } else {
+    }
+  } else if (!leader && warp == 1 && lane == 0) {
+    {
       // ---- follower: forward "my unit n is full" to the leader
       const uint32_t lead_peer = map_cluster(smem_u32(&c->peer[0]), rank - 1);
       join_cluster(joined);
@@ -665,6 +663,71 @@ __device__ void scorer(const VerifyArgs& a, const PoolMaps& maps, const Item& it
 }
 
 // ------------------------------------------------------------ accumulator
+// Accumulator epilogue: O_s = O / l as bf16 rows of the workspace, by eight
+// warps -- 4..7 (after the tile loop) write columns 0..255, 12..15 columns
+// 256..511 (a warp reaches the TMEM lanes of its index mod 4).  Each
+// 64-column slice goes TMEM -> registers -> its own 128-byte-swizzled 16 KB
+// box in the value ring (idle once the last PV completed) -> one TMA store,
+// which writes whole rows' slices coalesced and clips the rows past the
+// request.
+__device__ void acc_epilogue(const VerifyArgs& a, const PoolMaps& maps, const Item& it, uint8_t* sm, Ctrl* c) {
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int w = warp & 3, r = 32 * w + lane, hc = warp >= 12 ? 1 : 0;
+  const uint32_t lane_addr = c->tmem_base + ((uint32_t)(w * 32) << 16);
+  named_bar(3, 256);  // warps 12..15 wait here until warps 4..7 finished the tile loop
+  const bool done = wait_bar(&c->mma_done, 0, c, a.status);
+  const bool all_done = !named_bar_or(3, 256, !done);
+  tc_fence_after();
+  if (all_done) {
+    const float l = c->xmax[0][r];
+    const float inv = l > 0.f ? 1.f / l : 0.f;
+    constexpr int kBox = ROWS * 128;  // 16 KB
+#pragma unroll 1
+    for (int q = 4 * hc; q < 4 * hc + 4; ++q) {
+      uint8_t* box = sm + V_RING + q * kBox;
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        uint32_t v[32];
+        tmem_ld32(lane_addr + 64 * q + 32 * h, v);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {  // 16-byte piece 4h + j: columns 8 (4h + j) ..
+          uint32_t pk[4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            __nv_bfloat162 b2 = __floats2bfloat162_rn(__uint_as_float(v[8 * j + 2 * e]) * inv,
+                                                      __uint_as_float(v[8 * j + 2 * e + 1]) * inv);
+            pk[e] = *reinterpret_cast<uint32_t*>(&b2);
+          }
+          *reinterpret_cast<uint4*>(box + r * 128 + (((4 * h + j) ^ (r & 7)) << 4)) =
+              make_uint4(pk[0], pk[1], pk[2], pk[3]);
+        }
+      }
+    }
+    fence_async_smem();
+    named_bar(4 + hc, 128);
+    if (w == 0 && lane == 0 && it.row0 < a.rows_per_req) {
+      for (int q = 4 * hc; q < 4 * hc + 4; ++q)
+        asm volatile("cp.async.bulk.tensor.3d.global.shared::cta.tile.bulk_group [%0, {%1, %2, %3}], [%4];"
+                     ::"l"(&maps.po), "r"(64 * q), "r"(it.row0), "r"(it.slot), "r"(smem_u32(sm + V_RING + q * kBox))
+                     : "memory");
+      asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+      asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+      // The stores are read by other CTAs' ordinary loads in the fused merge.
+      asm volatile("fence.proxy.async;" ::: "memory");
+    }
+  } else if (hc == 0 && it.row0 + r < a.rows_per_req) {
+    for (int d = 0; d < kLatent; ++d)
+      a.partial_o[((size_t)it.slot * a.rows_per_req + it.row0 + r) * kLatent + d] = 0;
+  }
+}
+
+// Whether the P tile in buffer s asks for a rescale of O before its PV: the
+// softmax sets a flag word per warp when the running max of a row moved.
+__device__ __forceinline__ bool rescaled(const uint8_t* sm, int s) {
+  const uint32_t* flags = reinterpret_cast<const uint32_t*>(sm + V_PBUF + s * PBUF + PTILE + 384 * 4);
+  return (flags[0] | flags[1] | flags[2] | flags[3]) != 0u;
+}
+
 __device__ void accumulator(const VerifyArgs& a, const PoolMaps& maps, const Item& it, uint8_t* sm, Ctrl* c,
                             uint32_t rank, bool& joined) {
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -672,14 +735,15 @@ __device__ void accumulator(const VerifyArgs& a, const PoolMaps& maps, const Ite
   const bool leader = (rank & 1) == 0;
   const int par = rank & 1;            // value chunks 2q + par of every tile
   const uint32_t scorer_rank = rank - 2;
-  // Producer warps: load/store unit {0, 3, 8, 9}; TMA issuer 10 and
-  // forwarder 11 (contiguous runs).
+  // Producer warps: load/store unit {0, 3, 8, 9}; TMA issuer 10 (contiguous
+  // runs).  MMA issuers (leader): 1 (O columns 0..255), 11 (256..511).
   const int lsu = warp == 0 ? 0 : warp == 3 ? 1 : warp == 8 ? 2 : warp == 9 ? 3 : -1;
 
   if (warp == kLoaderWarp) {
     index_loader(a, it, sm, c);
   } else if (lsu >= 0) {
     constexpr int G = 32 / kLsuWarps;  // groups of four keys per warp (of the tile's 32)
+    uint32_t tpar = 0;                 // (warp 0) TMA phase parities, see tma_issuer
     for (int t = 0; t < it.ntiles; ++t) {
       const int s = t & 1;
       if (!wait_ring(a, c, t)) break;
@@ -698,6 +762,10 @@ __device__ void accumulator(const VerifyArgs& a, const PoolMaps& maps, const Ite
         for (int q = 0; q < 4; ++q) lsu_chunk<G>(a.kv_pool, slot + q * VCHUNK, 2 * q + par, 4 * G * lsu, ids, lane);
       }
       cp_async_mbar_arrive(&c->full[s]);
+      if (lsu == 0) {
+        if (lane == 0) ok = tma_count_in(a, c, contig, s, tpar);
+        if (!__shfl_sync(0xffffffffu, ok, 0)) break;
+      }
     }
     asm volatile("cp.async.wait_all;" ::: "memory");
   } else if (warp == 10 && lane == 0) {
@@ -710,25 +778,31 @@ __device__ void accumulator(const VerifyArgs& a, const PoolMaps& maps, const Ite
       if (load)
         for (int q = 0; q < 4; ++q) tma_run(&maps.tile, dst + q * VCHUNK, 2 * q + par, c->ifirst[t % NIDX], bar);
     });
-  } else if (warp == 11 && lane == 0) {
-    tma_forwarder(a, it, c, 1, VSLOTS);
-  } else if (warp == 1 && lane == 0) {
-    if (leader) {
-      // ---- MMA issuer for the pair: O[rows, 128q .. 128q+127] += P V
+  } else if (leader && (warp == 1 || warp == 11) && lane == 0) {
+    // ---- MMA issuers for the pair: O[rows, 128q .. 128q+127] += P V, warp 1
+    // for q = 0, 1 and warp 11 for q = 2, 3 (disjoint accumulator columns,
+    // so their MMAs need no order between them); each counts in on every
+    // tile's empty / pvdone barrier.
+    {
       constexpr uint32_t idesc = idesc_bf16_f32(256, 128, false, true);  // A = P K-major, B = V MN-major
+      const int q0 = warp == 1 ? 0 : 2;
       join_cluster(joined);
       for (int t = 0; t < it.ntiles; ++t) {
         const int s = t & 1;
         const uint32_t ph = (t >> 1) & 1;
+        // P and V of both CTAs in place (the follower's forward also covers
+        // its own rescale); this CTA's O rescaled first when the running max
+        // of any of its rows moved (flags in the P metadata).
         if (!wait_bar(&c->pfull[s], ph, c, a.status) || !wait_bar(&c->full[s], ph, c, a.status) ||
-            !wait_bar(&c->peer[s], ph, c, a.status) || !wait_bar(&c->corr_done[s], ph, c, a.status))
+            !wait_bar(&c->peer[s], ph, c, a.status) ||
+            (rescaled(sm, s) && !wait_bar(&c->corr_done[s], ph, c, a.status)))
           break;
         fence_async_smem();  // cp.async (generic proxy) data -> tensor-core reads
         tc_fence_after();
         const uint64_t pdesc = desc_sw128(smem_u32(sm + V_PBUF + s * PBUF), 16, 1024);
         const uint8_t* slot = sm + V_RING + s * VSLOT;
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
+        for (int q = q0; q < q0 + 2; ++q) {
           const uint64_t vdesc = desc_sw128(smem_u32(slot + q * VCHUNK), VCHUNK, 1024);
           // K steps 0..3 read P atom 0 (keys 0..63), 4..7 atom 1; V advances
           // 16 keys (2 KB) per step.
@@ -737,9 +811,12 @@ __device__ void accumulator(const VerifyArgs& a, const PoolMaps& maps, const Ite
         }
         commit2(&c->empty[s], kAccPair);
         commit2(&c->pvdone[s], kAccPair);
+        commit2(&c->pfree[s], kScorerPair);  // both scorers may refill P buffer s
       }
       commit2(&c->mma_done, kAccPair);
-    } else {
+    }
+  } else if (!leader && warp == 1 && lane == 0) {
+    {
       // ---- follower: forward "my P tile and my value slot of tile t are
       // both full" to the leader, as one arrive
       const uint32_t lead_peer = map_cluster(smem_u32(&c->peer[0]), rank - 1);
@@ -747,30 +824,24 @@ __device__ void accumulator(const VerifyArgs& a, const PoolMaps& maps, const Ite
       for (int t = 0; t < it.ntiles; ++t) {
         const int s = t & 1;
         const uint32_t ph = (t >> 1) & 1;
-        if (!wait_bar(&c->pfull[s], ph, c, a.status) || !wait_bar(&c->full[s], ph, c, a.status)) return;
+        if (!wait_bar(&c->pfull[s], ph, c, a.status) || !wait_bar(&c->full[s], ph, c, a.status) ||
+            (rescaled(sm, s) && !wait_bar(&c->corr_done[s], ph, c, a.status)))
+          return;
         fence_async_smem();
         signal_remote(lead_peer + s * 8);
       }
     }
-  } else if (warp == 2 && lane == 0) {
-    // ---- relay: PV of tile t finished -> re-arm P buffer s, release it to the scorer
-    const uint32_t sc_pfree = map_cluster(smem_u32(&c->pfree[0]), scorer_rank);
-    join_cluster(joined);
-    for (int s = 0; s < 2; ++s) mbar_arrive_expect_tx(&c->pfull[s], PCOPY);
-    for (int t = 0; t < it.ntiles; ++t) {
-      const int s = t & 1;
-      if (!wait_bar(&c->pvdone[s], (t >> 1) & 1, c, a.status)) break;
-      if (t + 2 < it.ntiles) mbar_arrive_expect_tx(&c->pfull[s], PCOPY);
-      signal_remote(sc_pfree + s * 8);
-    }
   } else if (warp >= 4 && warp < 8) {
-    // ---- correction + epilogue: thread = row r (TMEM lane r)
+    // ---- correction (then half of the epilogue): thread = row r (TMEM lane r)
     const int r = tid - 128;
     const int w = warp - 4;
     const uint32_t lane_addr = tmem + ((uint32_t)(w * 32) << 16);
     const uint32_t sc_pfree = map_cluster(smem_u32(&c->pfree[0]), scorer_rank);
-    const uint32_t lead_corr = map_cluster(smem_u32(&c->corr_done[0]), rank & ~1u);
     join_cluster(joined);
+    // P buffers 0 and 1 expect their first copies (later phases are armed
+    // below, once the previous phase was seen complete).
+    if (r == 0)
+      for (int s = 0; s < 2 && s < it.ntiles; ++s) mbar_arrive_expect_tx(&c->pfull[s], PCOPY);
     float lfin = 0.f;
     for (int t = 0; t < it.ntiles; ++t) {
       const int s = t & 1;
@@ -797,71 +868,22 @@ __device__ void accumulator(const VerifyArgs& a, const PoolMaps& maps, const Ite
         }
         tc_fence_before();
       }
-      // Every tile: this CTA's O is ready for PV(t) (the leader counts 8 warps).
+      // Every tile: this CTA's O is ready for PV(t) (waited for only when
+      // the flags asked for a rescale).
       __syncwarp();
-      if (lane == 0) signal_remote(lead_corr + s * 8);
-      // Second release of P buffer s: its metadata has been read.
+      if (lane == 0) mbar_arrive(&c->corr_done[s]);
+      // P buffer s: its metadata has been read (the scorer's third release,
+      // after the two MMA issuers' commits), and its next phase may be armed.
       const bool stop = named_bar_or(2, 128, aborted(c));
-      if (r == 0 && !stop) release_remote(sc_pfree + s * 8);
+      if (r == 0 && !stop) {
+        if (t + 2 < it.ntiles) mbar_arrive_expect_tx(&c->pfull[s], PCOPY);
+        release_remote(sc_pfree + s * 8);
+      }
       if (stop) break;
     }
-    // Epilogue: O_s = O / l, written as bf16 rows of the workspace.  Each
-    // 64-column slice of the tile goes TMEM -> registers -> a swizzled
-    // shared-memory box (4 rotating 16 KB boxes in the free value ring) ->
-    // one TMA store, which writes whole rows' slices coalesced and clips
-    // the rows past the request.
-    const bool done = wait_bar(&c->mma_done, 0, c, a.status);
-    tc_fence_after();
-    const int req_row = it.row0 + r;
-    const bool row_ok = req_row < a.rows_per_req;
-    if (__all_sync(0xffffffffu, done)) {
-      const float inv = lfin > 0.f ? 1.f / lfin : 0.f;
-      const bool store = it.row0 < a.rows_per_req;
-      constexpr int kBox = ROWS * 128;  // 16 KB
-      for (int q = 0; q < kLatent / 64; ++q) {
-        uint8_t* box = sm + V_RING + (q & 3) * kBox;
-        if (q >= 4) {
-          // The store issued from this box four slices ago must have read it.
-          if (r == 0) asm volatile("cp.async.bulk.wait_group.read 3;" ::: "memory");
-          named_bar(2, 128);
-        }
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          uint32_t v[32];
-          tmem_ld32(lane_addr + 64 * q + 32 * h, v);
-#pragma unroll
-          for (int j = 0; j < 4; ++j) {  // 16-byte piece 4h + j: columns 8 (4h + j) ..
-            uint32_t pk[4];
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              __nv_bfloat162 b2 = __floats2bfloat162_rn(__uint_as_float(v[8 * j + 2 * e]) * inv,
-                                                        __uint_as_float(v[8 * j + 2 * e + 1]) * inv);
-              pk[e] = *reinterpret_cast<uint32_t*>(&b2);
-            }
-            *reinterpret_cast<uint4*>(box + r * 128 + (((4 * h + j) ^ (r & 7)) << 4)) =
-                make_uint4(pk[0], pk[1], pk[2], pk[3]);
-          }
-        }
-        fence_async_smem();
-        named_bar(2, 128);
-        if (r == 0 && store) {
-          asm volatile(
-              "cp.async.bulk.tensor.3d.global.shared::cta.tile.bulk_group [%0, {%1, %2, %3}], [%4];\n"
-              "cp.async.bulk.commit_group;" ::"l"(&maps.po), "r"(64 * q), "r"(it.row0), "r"(it.slot),
-              "r"(smem_u32(box))
-              : "memory");
-        }
-      }
-      if (r == 0) {
-        asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
-        // The stores are read by other CTAs' ordinary loads in the fused merge.
-        asm volatile("fence.proxy.async;" ::: "memory");
-      }
-    } else if (row_ok) {
-      for (int d = 0; d < kLatent; ++d)
-        a.partial_o[((size_t)it.slot * a.rows_per_req + req_row) * kLatent + d] = 0;
-    }
+    c->xmax[0][r] = lfin;  // the row's final l, for the epilogue (published by its barrier)
   }
+  if ((warp >= 4 && warp < 8) || warp >= 12) acc_epilogue(a, maps, it, sm, c);
 }
 
 __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(kThreads, 1)
@@ -888,19 +910,18 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(kThreads, 1)
   const bool work = have && it.ntiles > 0;
   if (tid == 0) {
     for (int i = 0; i < kMaxSlots; ++i) {
-      mbar_init(&c->full[i], 32 * kLsuWarps + 1);  // every load/store-unit lane, the TMA forwarder
+      mbar_init(&c->full[i], 32 * kLsuWarps + 1);  // every load/store-unit lane, the TMA stream
       mbar_init(&c->peer[i], 1);
-      mbar_init(&c->empty[i], 1);
+      mbar_init(&c->empty[i], rank < 2 ? 1 : 2);  // accumulator: both MMA issuers commit
       mbar_init(&c->tma[i], 1);
     }
-    c->tma_issued = 0;
     for (int i = 0; i < 2; ++i) {
       mbar_init(&c->sfull[i], 1);
       mbar_init(&c->sempty[i], 16);
-      mbar_init(&c->pfree[i], 2);
+      mbar_init(&c->pfree[i], 3);  // two PV commits + the metadata release
       mbar_init(&c->pfull[i], 1);
-      mbar_init(&c->pvdone[i], 1);
-      mbar_init(&c->corr_done[i], 8);
+      mbar_init(&c->pvdone[i], 2);
+      mbar_init(&c->corr_done[i], 4);
     }
     // Index ring: the loader's 32 lanes fill a slot; it is released by every
     // producer warp, and in the scorers also by the eight softmax warps.
@@ -908,7 +929,7 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(kThreads, 1)
       mbar_init(&c->ifull[i], 32);
       mbar_init(&c->iempty[i], kLsuWarps + 1 + (rank < 2 ? 8 : 0));
     }
-    mbar_init(&c->mma_done, 1);
+    mbar_init(&c->mma_done, 2);  // two MMA issuers per pair
     mbar_init(&c->q_ready, 8);
     mbar_init(&c->qload, 1);
     c->abort = 0;
@@ -978,7 +999,7 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(kThreads, 1)
         if (v >= gridDim.x) break;
         if (spin == 4u) {
           deadline = global_timer_ns() + a.wait_ns;
-        } else if ((spin & 63u) == 0u && global_timer_ns() > deadline) {
+        } else if (spin > 4u && (spin & 7u) == 0u && global_timer_ns() > deadline) {
           ok = false;
           break;
         }

@@ -65,10 +65,11 @@ __device__ __forceinline__ bool mbar_try_wait_cluster(uint64_t* bar, uint32_t pa
       : "memory");
   return ok != 0;
 }
-// Bounded wait on a phase: false once about `limit_ns` (global timer) have
-// passed.  The timer is first read after four unsuccessful tries, then every
-// 64: a timer read costs far more than a try, and most waits here find the
-// phase already complete.
+// Bounded wait on a phase: false once `limit_ns` (global timer) have passed.
+// The first four tries go without the timer (a timer read costs far more than
+// a try, and most waits here find the phase complete at once); after that the
+// wait is a long one and the deadline is checked after every try (a try may
+// itself suspend the thread for a while).
 template <bool kCluster>
 __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity, uint64_t limit_ns) {
   uint64_t deadline = 0;
@@ -76,7 +77,7 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity
     if (kCluster ? mbar_try_wait_cluster(bar, parity) : mbar_try_wait(bar, parity)) return true;
     if (it == 4u) {
       deadline = global_timer_ns() + limit_ns;
-    } else if ((it & 63u) == 0u && global_timer_ns() > deadline) {
+    } else if (it > 4u && global_timer_ns() > deadline) {
       return false;
     }
   }
