@@ -270,6 +270,8 @@ int run(const ddtree_plan_t* p, const uint16_t* q_latent, const uint16_t* q_rope
   a.partial_lse = reinterpret_cast<float*>(ws + p->off_partial_lse);
   a.partial_o = reinterpret_cast<uint16_t*>(ws + p->off_partial_o);
   a.fused = p->fused_combine;
+  // Every request has at most ceil(max_keys / chunk) splits.
+  a.merge_depth = merge_depth_for(a.fused, p->max_keys, p->chunk_keys);
   a.wait_ns = p->wait_limit_us > 0 ? (uint64_t)p->wait_limit_us * 1000ull : 2000000000ull;
   a.pool_rows = p->pool_rows;
   a.sm_scale = sm_scale;

@@ -14,6 +14,15 @@ namespace ddtree {
 constexpr int kLatent = DDTREE_LATENT_DIM;  // 512: value width
 constexpr int kRope = DDTREE_ROPE_DIM;      // 64
 constexpr int kRow = DDTREE_ROW_DIM;        // 576: key width
+// The fused split merge loads a request's splits for two rows in one tile
+// box (2 KB of shared memory per split) when there are at most this many.
+constexpr int kMergeMaxSplits = 64;
+// Splits per merge box for a plan (0: merge by warps instead).
+inline int merge_depth_for(int fused, int max_keys, int chunk_keys) {
+  if (!fused || chunk_keys <= 0) return 0;
+  const long long d = ((long long)max_keys + chunk_keys - 1) / chunk_keys;
+  return (d >= 1 && d <= kMergeMaxSplits) ? (int)d : 0;
+}
 
 // Everything a launch needs, resolved on the host from the plan and the
 // caller's pointers.  Passed by value as a kernel parameter.
@@ -38,6 +47,7 @@ struct VerifyArgs {
   int32_t tile_keys, chunk_keys, total_splits, row_tile, row_tiles;
   int32_t q_lat_stride, q_rope_stride;
   int32_t fused;               // the partial kernel merges the splits itself
+  int32_t merge_depth;         // fused merge by tile loads: splits per box (0: by warps)
   uint64_t wait_ns;            // bound of every wait inside the kernels
 };
 

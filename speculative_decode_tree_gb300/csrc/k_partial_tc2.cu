@@ -89,9 +89,11 @@ constexpr int Q_RING = Q_ROPE + VCHUNK;                 // scorer: 7 x 24 KB
 constexpr int Q_STAGE = Q_RING + QSLOTS * QUNIT;        // scorer: P staging
 constexpr int Q_END = Q_STAGE + PBUF;
 // Q latent (128 rows x 512 bf16, eight 64-column 128-byte-swizzled boxes)
-// lands by TMA in ring slots 2.. and the start of the P staging buffer,
-// before any of them is used; the softmax warps move it into TMEM.
-constexpr int Q_LAT_STAGE = Q_RING + 2 * QUNIT;
+// lands by TMA in ring slots 3.. and most of the P staging buffer, before
+// any of them is used (the first tile's three units need only slots 0..2);
+// the softmax warps move it into TMEM.
+constexpr int kQStageSlot = 3;
+constexpr int Q_LAT_STAGE = Q_RING + kQStageSlot * QUNIT;
 constexpr int Q_LAT_BYTES = ROWS * kLatent * 2;
 constexpr int Q_ROPE_BYTES = ROWS * kRope * 2;
 static_assert(Q_LAT_STAGE + Q_LAT_BYTES <= Q_END, "Q latent staging fits the unused ring");
@@ -122,6 +124,7 @@ struct __align__(8) Ctrl {
   uint64_t mma_done;
   uint64_t q_ready;   // scorer: Q latent in TMEM and Q rope in shared memory
   uint64_t qload;     // scorer: the TMA loads of Q (latent staging + rope) landed
+  uint64_t mload;     // fused merge: a unit's partials landed
   uint64_t wait_ns;        // bound of the waits (the caller's, default 2 s)
   uint32_t tmem_base;
   uint32_t abort;
@@ -242,6 +245,7 @@ struct PoolMaps {
   CUtensorMap po;     // partial O [splits][rows_per_req][512] bf16, 64 columns x 128 rows box
   CUtensorMap ql;     // Q latent [B*T*H rows][512] bf16, 64 columns x 128 rows box
   CUtensorMap qr;     // Q rope [B*T*H rows][64] bf16, 64 columns x 128 rows box
+  CUtensorMap pm;     // partial O again, unswizzled box of 256 columns x 2 rows x merge_depth splits
 };
 
 // The start-of-kernel cluster barrier is split: every thread arrives once its
@@ -350,13 +354,13 @@ __device__ __forceinline__ void tma_run(const CUtensorMap* map, uint8_t* dst, in
 // Lane 0 of load/store-unit warp 0 counts the stream in on the slot's full
 // barrier: at once for a scattered unit (no TMA bytes), once the bytes landed
 // for a contiguous one.  Both sides track the phase parity of each slot's
-// TMA barrier from the same per-tile flags.  A non-null `gate2` is waited for
-// (phase 0) before unit 2 is loaded.  Only the last load started on a slot
+// TMA barrier from the same per-tile flags.  A non-null `gate` is waited for
+// (phase 0) before unit kQStageSlot is loaded.  Only the last load started on a slot
 // can still be in flight (an earlier one was consumed before its slot was
 // reused), so before it leaves the issuer waits (fixed bound) for those.
 template <typename Issue>
 __device__ __forceinline__ void tma_issuer(const VerifyArgs& a, const Item& it, Ctrl* c, int upt, int nslots,
-                                           uint64_t* gate2, Issue&& issue) {
+                                           uint64_t* gate, Issue&& issue) {
   uint32_t par = 0, armed = 0;  // per slot: parity of the next TMA phase; a load was started
   const int nunits = it.ntiles * upt;
   for (int n = 0; n < nunits; ++n) {
@@ -364,7 +368,7 @@ __device__ __forceinline__ void tma_issuer(const VerifyArgs& a, const Item& it, 
     if (u == 0 && !wait_ring(a, c, t)) break;
     bool free = true;
     if (c->icontig[t % NIDX] != 0) {
-      free = (n != 2 || gate2 == nullptr || wait_bar(gate2, 0, c, a.status)) &&
+      free = (n != kQStageSlot || gate == nullptr || wait_bar(gate, 0, c, a.status)) &&
              wait_bar(&c->empty[slot], ((n / nslots) & 1) ^ 1, c, a.status);
       if (free) {
         issue(n, t, u, slot, &c->tma[slot]);
@@ -416,10 +420,10 @@ __device__ void scorer(const VerifyArgs& a, const PoolMaps& maps, const Item& it
       bool ok = true;
       for (int u = 0; u < 3 && ok; ++u) {
         const int n = 3 * t + u, slot = n % QSLOTS;
-        // Slots 2.. hold the Q latent staging until the softmax warps moved
-        // it into TMEM (q_ready).
+        // Slots kQStageSlot.. hold the Q latent staging until the softmax
+        // warps moved it into TMEM (q_ready).
         if (lane == 0)
-          ok = (n != 2 || wait_bar(&c->q_ready, 0, c, a.status)) &&
+          ok = (n != kQStageSlot || wait_bar(&c->q_ready, 0, c, a.status)) &&
                wait_bar(&c->empty[slot], ((n / QSLOTS) & 1) ^ 1, c, a.status);
         ok = __shfl_sync(0xffffffffu, ok, 0);
         if (!ok) break;
@@ -886,6 +890,85 @@ __device__ void accumulator(const VerifyArgs& a, const PoolMaps& maps, const Ite
   if ((warp >= 4 && warp < 8) || warp >= 12) acc_epilogue(a, maps, it, sm, c);
 }
 
+// ------------------------------------------------------------ fused merge
+// The split merge by tile loads (after the grid barrier): a unit is two rows
+// of one request; one thread loads all of the request's split partials for
+// them (two boxes of 256 columns x 2 rows x merge_depth splits, 2 KB per
+// split) into shared memory, two warps turn the rows' split LSEs into
+// weights, and every thread merges two columns of one row:
+//     lse = ln sum_s exp(lse_s),   O = sum_s exp(lse_s - lse) O_s.
+// `zero` writes zero rows and -inf LSEs (untrusted partials).
+__device__ void tile_merge(const VerifyArgs& a, const PoolMaps& maps, uint8_t* sm, Ctrl* c, bool zero) {
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int D = a.merge_depth;
+  const int pairs = (a.rows_per_req + 1) >> 1;
+  const int units = a.batch * pairs;
+  const uint32_t box_bytes = 256u * 2u * (uint32_t)D * 2u;
+  float* wgt = c->xmax[0];  // [2 rows][64 splits] weights
+  float* rowl = c->xmax[1]; // [2 rows]: l, then lse
+  uint32_t ph = 0;
+  for (int u = blockIdx.x; u < units; u += gridDim.x, ph ^= 1u) {
+    const int b = u / pairs, r0 = 2 * (u - b * pairs);
+    int first = 0, count = 0;
+    combine_slots(a, b * a.rows_per_req * kCombineUnitsPerRow, lane, first, count);
+    count = zero ? 0 : min(count, D);
+    if (tid == 0 && count > 0) {
+      // The partials were written by other CTAs' TMA stores, seen through
+      // the grid barrier (generic proxy); these loads are async proxy.
+      asm volatile("fence.proxy.async.global;" ::: "memory");
+      mbar_arrive_expect_tx(&c->mload, 2 * box_bytes);
+      for (int h = 0; h < 2; ++h)
+        asm volatile(
+            "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], [%5];"
+            ::"r"(smem_u32(sm + h * box_bytes)), "l"(&maps.pm), "r"(256 * h), "r"(r0), "r"(first), "r"(smem_u32(&c->mload))
+            : "memory");
+    }
+    if (warp < 2) {  // warp w: the weights of row r0 + w (lane j: splits j, j + 32)
+      const int row = r0 + warp;
+      const bool live = row < a.rows_per_req;
+      const float* pl = a.partial_lse + (size_t)first * a.rows_per_req + (live ? row : 0);
+      const float la = (live && lane < count) ? __ldcg(pl + (size_t)lane * a.rows_per_req) : -INFINITY;
+      const float lb = (live && lane + 32 < count) ? __ldcg(pl + (size_t)(lane + 32) * a.rows_per_req) : -INFINITY;
+      float m = fmaxf(la, lb);
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+      const float wa = la == -INFINITY ? 0.f : __expf(la - m);
+      const float wb = lb == -INFINITY ? 0.f : __expf(lb - m);
+      float l = wa + wb;
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) l += __shfl_xor_sync(0xffffffffu, l, o);
+      const float inv = l > 0.f ? 1.f / l : 0.f;
+      wgt[64 * warp + lane] = wa * inv;
+      wgt[64 * warp + lane + 32] = wb * inv;
+      if (lane == 0) rowl[warp] = l > 0.f ? m + logf(l) : -INFINITY;
+    }
+    __syncthreads();
+    bool ok = true;
+    if (count > 0) ok = mbar_wait(&c->mload, ph, a.wait_ns);
+    if (!ok && tid == 0) atomicOr(a.status, DDTREE_ST_TIMEOUT);
+    // thread: row r0 + (tid >> 8), columns 2 (tid & 255) .. + 1
+    const int rr = tid >> 8, col = 2 * (tid & 255);
+    const int row = r0 + rr;
+    if (row < a.rows_per_req) {
+      const int h = col >> 8;
+      const uint8_t* src = sm + h * box_bytes + rr * 512 + (col & 255) * 2;
+      float acc0 = 0.f, acc1 = 0.f;
+      if (ok)
+        for (int s = 0; s < count; ++s) {
+          const float w = wgt[64 * rr + s];
+          const uint32_t x = *reinterpret_cast<const uint32_t*>(src + (size_t)s * 1024);
+          acc0 = fmaf(w, bf16_lo(x), acc0);
+          acc1 = fmaf(w, bf16_hi(x), acc1);
+        }
+      const size_t g = (size_t)b * a.rows_per_req + row;
+      *reinterpret_cast<__nv_bfloat162*>(a.out + g * kLatent + col) = __floats2bfloat162_rn(acc0, acc1);
+      if ((tid & 255) == 0) a.lse[g] = ok ? rowl[rr] : -INFINITY;
+    }
+    __syncthreads();  // the boxes and weights are reused by the next unit
+    if (count == 0) ph ^= 1u;  // no load this unit: the barrier did not move
+  }
+}
+
 __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(kThreads, 1)
     partial_tc2_kernel(const VerifyArgs a, const __grid_constant__ PoolMaps maps) {
   extern __shared__ uint8_t smem_raw[];
@@ -932,6 +1015,7 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(kThreads, 1)
     mbar_init(&c->mma_done, 2);  // two MMA issuers per pair
     mbar_init(&c->q_ready, 8);
     mbar_init(&c->qload, 1);
+    mbar_init(&c->mload, 1);
     c->abort = 0;
     c->wait_ns = a.wait_ns;
     fence_mbar_init();
@@ -954,8 +1038,10 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(kThreads, 1)
   tc_fence_after();
 
   // This CTA's barriers and TMEM are ready for the others; each thread waits
-  // for theirs before its first remote action (join_cluster).
-  asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+  // for theirs before its first remote action (join_cluster).  Relaxed: the
+  // barrier initialisation was published by its own fence, and nothing else
+  // written so far is read by another CTA.
+  asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
   bool joined = false;
   if (work) {
     if (rank < 2) scorer(a, maps, it, sm, c, rank, joined);
@@ -987,7 +1073,7 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(kThreads, 1)
     const int stride = gridDim.x * (kThreads / 32);
     int u = blockIdx.x * (kThreads / 32) + warp;
     int first = 0, count = 0;
-    if (u < units) combine_slots(a, u, tid & 31, first, count);
+    if (a.merge_depth == 0 && u < units) combine_slots(a, u, tid & 31, first, count);
     if (tid == 0) {
       __threadfence();
       atomicAdd(a.grid_done, 1u);
@@ -1011,6 +1097,10 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(kThreads, 1)
     }
     __syncthreads();
     const bool zero = c->merge_zero != 0;
+    if (a.merge_depth > 0) {
+      tile_merge(a, maps, sm, c, zero);
+      return;
+    }
     for (; u < units; u += stride) {
       combine_unit(a, u, tid & 31, first, zero ? 0 : count);
       if (u + stride < units) combine_slots(a, u + stride, tid & 31, first, count);
@@ -1067,6 +1157,15 @@ cudaError_t make_pool_maps(const VerifyArgs& a, PoolMaps* m) {
           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
     return cudaErrorInvalidValue;
+  // The fused merge's view of the partials: two rows x 256 columns of up to
+  // merge_depth consecutive splits per box (splits past the last read zeros).
+  if (a.merge_depth > 0) {
+    const cuuint32_t mbox[3] = {256, 2, (cuuint32_t)a.merge_depth};
+    if (enc(&m->pm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, a.partial_o, odims, ostrides, mbox, oes,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return cudaErrorInvalidValue;
+  }
   // Queries: rows (t, h) of all requests, request-major; rows past the last
   // one read as zeros.  The row strides are multiples of 8 elements and the
   // bases 16-byte aligned (checked when the call is validated).

@@ -133,6 +133,7 @@ extern "C" int ddtree_verify_mla_noalloc(const ddtree_bf16_t* q_latent, const dd
   a.partial_lse = reinterpret_cast<float*>(ws + plan.off_partial_lse);
   a.partial_o = reinterpret_cast<uint16_t*>(ws + plan.off_partial_o);
   a.fused = plan.fused_combine;
+  a.merge_depth = merge_depth_for(a.fused, plan.max_keys, plan.chunk_keys);
   a.wait_ns = 2000000000ull;
   a.pool_rows = 0;
   a.sm_scale = sm_scale;
