@@ -898,19 +898,26 @@ __device__ void accumulator(const VerifyArgs& a, const PoolMaps& maps, const Ite
 // weights, and every thread merges two columns of one row:
 //     lse = ln sum_s exp(lse_s),   O = sum_s exp(lse_s - lse) O_s.
 // `zero` writes zero rows and -inf LSEs (untrusted partials).
-__device__ void tile_merge(const VerifyArgs& a, const PoolMaps& maps, uint8_t* sm, Ctrl* c, bool zero) {
+__device__ __forceinline__ int tile_merge_units(const VerifyArgs& a) { return a.batch * ((a.rows_per_req + 1) >> 1); }
+// The split range of tile-merge unit u (two rows of request u / pairs).
+__device__ __forceinline__ void tile_merge_slots(const VerifyArgs& a, int u, int& first, int& count) {
+  const int b = u / ((a.rows_per_req + 1) >> 1);
+  combine_slots(a, b * a.rows_per_req * kCombineUnitsPerRow, threadIdx.x & 31, first, count);
+}
+// (first, count): the slots of this CTA's first unit, looked up in advance.
+__device__ void tile_merge(const VerifyArgs& a, const PoolMaps& maps, uint8_t* sm, Ctrl* c, bool zero, int first,
+                           int count) {
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int D = a.merge_depth;
   const int pairs = (a.rows_per_req + 1) >> 1;
-  const int units = a.batch * pairs;
+  const int units = tile_merge_units(a);
   const uint32_t box_bytes = 256u * 2u * (uint32_t)D * 2u;
   float* wgt = c->xmax[0];  // [2 rows][64 splits] weights
   float* rowl = c->xmax[1]; // [2 rows]: l, then lse
   uint32_t ph = 0;
   for (int u = blockIdx.x; u < units; u += gridDim.x, ph ^= 1u) {
     const int b = u / pairs, r0 = 2 * (u - b * pairs);
-    int first = 0, count = 0;
-    combine_slots(a, b * a.rows_per_req * kCombineUnitsPerRow, lane, first, count);
+    if (u != (int)blockIdx.x) tile_merge_slots(a, u, first, count);
     count = zero ? 0 : min(count, D);
     if (tid == 0 && count > 0) {
       // The partials were written by other CTAs' TMA stores, seen through
@@ -1069,14 +1076,20 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(kThreads, 1)
     // (row, 64-column) merge units.  A timed-out wait anywhere writes zeros.
     // Each warp looks up its first unit's split range while the grid
     // finishes.
+    const bool by_tiles = a.merge_depth > 0;
     const int units = combine_units(a);
     const int stride = gridDim.x * (kThreads / 32);
     int u = blockIdx.x * (kThreads / 32) + warp;
     int first = 0, count = 0;
-    if (a.merge_depth == 0 && u < units) combine_slots(a, u, tid & 31, first, count);
+    if (by_tiles) {
+      if ((int)blockIdx.x < tile_merge_units(a)) tile_merge_slots(a, blockIdx.x, first, count);
+    } else if (u < units) {
+      combine_slots(a, u, tid & 31, first, count);
+    }
     if (tid == 0) {
-      __threadfence();
-      atomicAdd(a.grid_done, 1u);
+      // Release: this CTA's partials (stored before the cluster barrier
+      // above) are visible to whoever sees the count.
+      asm volatile("red.release.gpu.global.add.u32 [%0], 1;" ::"l"(a.grid_done) : "memory");
       uint64_t deadline = 0;
       bool ok = true;
       for (uint32_t spin = 1;; ++spin) {
@@ -1097,8 +1110,8 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(kThreads, 1)
     }
     __syncthreads();
     const bool zero = c->merge_zero != 0;
-    if (a.merge_depth > 0) {
-      tile_merge(a, maps, sm, c, zero);
+    if (by_tiles) {
+      tile_merge(a, maps, sm, c, zero, first, count);
       return;
     }
     for (; u < units; u += stride) {
