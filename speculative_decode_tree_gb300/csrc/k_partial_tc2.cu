@@ -75,7 +75,12 @@ constexpr int PCOPY = PTILE + META;      // bytes shipped per tile (multiple of 
 constexpr int PBUF = 34816;              // P buffer stride (1024-aligned)
 constexpr int NIDX = 8;                  // index ring: tiles of indices held ahead
 constexpr int kThreads = 512;            // 16 warps
-constexpr int kLsuWarps = 4;             // producer warps on the load/store unit (cp.async)
+// Producer warps on the load/store unit (cp.async): the gather rate of an SM
+// grows with the warps issuing (about 18 / 33 / 47 GB/s per SM with 4 / 8 / 16
+// warps in a probe), so every warp a role can spare gathers.
+constexpr int kScLsuWarps = 4;           // scorer CTAs
+constexpr int kAccLsuWarps = 8;          // accumulator CTAs
+__host__ __device__ constexpr int lsu_warps(uint32_t rank) { return rank < 2 ? kScLsuWarps : kAccLsuWarps; }
 constexpr int kLoaderWarp = 15;
 constexpr float kLazyRescale = 8.0f;     // rescale only when the max grows by > 2^8 (log2 units)
 // Tensor-core work must be complete before TMEM is freed: this wait keeps a
@@ -407,7 +412,7 @@ __device__ void scorer(const VerifyArgs& a, const PoolMaps& maps, const Item& it
   if (warp == kLoaderWarp) {
     index_loader(a, it, sm, c);
   } else if (lsu >= 0) {
-    constexpr int G = 16 / kLsuWarps;  // groups of four keys per warp (of the half's 16)
+    constexpr int G = 16 / kScLsuWarps;  // groups of four keys per warp (of the half's 16)
     uint32_t tpar = 0;                 // (warp 0) TMA phase parities, see tma_issuer
     for (int t = 0; t < it.ntiles; ++t) {
       if (!wait_ring(a, c, t)) break;
@@ -739,14 +744,16 @@ __device__ void accumulator(const VerifyArgs& a, const PoolMaps& maps, const Ite
   const bool leader = (rank & 1) == 0;
   const int par = rank & 1;            // value chunks 2q + par of every tile
   const uint32_t scorer_rank = rank - 2;
-  // Producer warps: load/store unit {0, 3, 8, 9}; TMA issuer 10 (contiguous
-  // runs).  MMA issuers (leader): 1 (O columns 0..255), 11 (256..511).
-  const int lsu = warp == 0 ? 0 : warp == 3 ? 1 : warp == 8 ? 2 : warp == 9 ? 3 : -1;
+  // Producer warps: load/store unit {0, 2, 3, 8, 9, 12, 13, 14} (12..14 then
+  // join the epilogue); TMA issuer 10 (contiguous runs).  MMA issuers
+  // (leader): 1 (O columns 0..255), 11 (256..511).
+  const int lsu = warp == 0 ? 0 : warp == 2 ? 1 : warp == 3 ? 2 : warp == 8 ? 3 : warp == 9 ? 4
+                : (warp >= 12 && warp <= 14) ? warp - 7 : -1;
 
   if (warp == kLoaderWarp) {
     index_loader(a, it, sm, c);
   } else if (lsu >= 0) {
-    constexpr int G = 32 / kLsuWarps;  // groups of four keys per warp (of the tile's 32)
+    constexpr int G = 32 / kAccLsuWarps;  // groups of four keys per warp (of the tile's 32)
     uint32_t tpar = 0;                 // (warp 0) TMA phase parities, see tma_issuer
     for (int t = 0; t < it.ntiles; ++t) {
       const int s = t & 1;
@@ -1000,7 +1007,7 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(kThreads, 1)
   const bool work = have && it.ntiles > 0;
   if (tid == 0) {
     for (int i = 0; i < kMaxSlots; ++i) {
-      mbar_init(&c->full[i], 32 * kLsuWarps + 1);  // every load/store-unit lane, the TMA stream
+      mbar_init(&c->full[i], 32 * lsu_warps(rank) + 1);  // every load/store-unit lane, the TMA stream
       mbar_init(&c->peer[i], 1);
       mbar_init(&c->empty[i], rank < 2 ? 1 : 2);  // accumulator: both MMA issuers commit
       mbar_init(&c->tma[i], 1);
@@ -1017,7 +1024,7 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(kThreads, 1)
     // producer warp, and in the scorers also by the eight softmax warps.
     for (int i = 0; i < NIDX; ++i) {
       mbar_init(&c->ifull[i], 32);
-      mbar_init(&c->iempty[i], kLsuWarps + 1 + (rank < 2 ? 8 : 0));
+      mbar_init(&c->iempty[i], lsu_warps(rank) + 1 + (rank < 2 ? 8 : 0));
     }
     mbar_init(&c->mma_done, 2);  // two MMA issuers per pair
     mbar_init(&c->q_ready, 8);
