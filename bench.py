@@ -103,7 +103,7 @@ def _peaks():
 # when it was taken (profiles/ has the summaries and commands).  Any other
 # version of the source reports null.
 TRAFFIC = {
-    "k_partial_tc2.cu": ("e3f3e3b4f86edaa3895ab9949dacadece8f600c6", 76247808 + 2372608),
+    "k_partial_tc2.cu": ("159c51454807b90bb4fb3846ceebe465e98334ed", 76240128 + 2551040),
     "k_accept.cu": ("016411fbe872d42040beebcfdb04b0f2d27eef9e", 8556032),
     "k_mask.cu": ("35de2ba635e46a78af91ca088bc100827946414a", 2114000),
     # mark + check + copy of one relocate_long call
