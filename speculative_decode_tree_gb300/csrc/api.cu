@@ -187,8 +187,12 @@ extern "C" int ddtree_verify_mla_plan_ex(int batch, int n_nodes, int n_heads,
   if (splits > INT32_MAX / 4) return DDTREE_EINVAL;
   p.total_splits = (int32_t)splits;
   // The cluster-of-four kernel merges the splits itself (no second launch)
-  // when all of its clusters are resident at once on this device.
-  p.fused_combine = (p.kernel == DDTREE_KERNEL_TC2 && device_sized && items_for(chunk) <= target_items) ? 1 : 0;
+  // when all of its clusters are resident at once on this device and a
+  // request's splits fit one tile load of its merge.
+  p.fused_combine = (p.kernel == DDTREE_KERNEL_TC2 && device_sized && items_for(chunk) <= target_items &&
+                     merge_depth_for(1, (int)max_keys, (int)chunk) > 0)
+                        ? 1
+                        : 0;
 
   p.off_partial_lse = kStatusBytes;
   p.off_partial_o = p.off_partial_lse + partial_lse_bytes(splits, p.rows_per_req);
@@ -228,7 +232,9 @@ int validate_plan(const ddtree_plan_t* p) {
   if (p->off_partial_lse != kStatusBytes || p->off_partial_o != kStatusBytes + lse_bytes ||
       p->workspace_bytes != p->off_partial_o + o_bytes)
     return DDTREE_EINVAL;
-  if (p->fused_combine != 0 && (p->fused_combine != 1 || p->kernel != DDTREE_KERNEL_TC2)) return DDTREE_EINVAL;
+  if (p->fused_combine != 0 && (p->fused_combine != 1 || p->kernel != DDTREE_KERNEL_TC2 ||
+                                merge_depth_for(1, p->max_keys, p->chunk_keys) == 0))
+    return DDTREE_EINVAL;
   if (p->wait_limit_us < 0) return DDTREE_EINVAL;
   int ls = p->q_latent_row_stride, rs = p->q_rope_row_stride;
   if (ls != 0 && (ls < kLatent || ls % 8)) return DDTREE_EINVAL;

@@ -1079,20 +1079,13 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(kThreads, 1)
   if (a.fused) {
     // Merge the splits in this launch: every CTA of the grid is resident at
     // once (cooperative launch), so each counts itself done and waits,
-    // bounded, for all others; then the warps of the grid share the
-    // (row, 64-column) merge units.  A timed-out wait anywhere writes zeros.
-    // Each warp looks up its first unit's split range while the grid
+    // bounded, for all others; then each CTA merges two rows at a time from
+    // one tile load of all their splits (the plan fuses only when a
+    // request's splits fit it).  A timed-out wait anywhere writes zeros.
+    // The split range of the CTA's first unit is looked up while the grid
     // finishes.
-    const bool by_tiles = a.merge_depth > 0;
-    const int units = combine_units(a);
-    const int stride = gridDim.x * (kThreads / 32);
-    int u = blockIdx.x * (kThreads / 32) + warp;
     int first = 0, count = 0;
-    if (by_tiles) {
-      if ((int)blockIdx.x < tile_merge_units(a)) tile_merge_slots(a, blockIdx.x, first, count);
-    } else if (u < units) {
-      combine_slots(a, u, tid & 31, first, count);
-    }
+    if ((int)blockIdx.x < tile_merge_units(a)) tile_merge_slots(a, blockIdx.x, first, count);
     if (tid == 0) {
       // Release: this CTA's partials (stored before the cluster barrier
       // above) are visible to whoever sees the count.
@@ -1116,15 +1109,7 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(kThreads, 1)
       c->merge_zero = (!ok || (st & DDTREE_ST_TIMEOUT)) ? 1u : 0u;
     }
     __syncthreads();
-    const bool zero = c->merge_zero != 0;
-    if (by_tiles) {
-      tile_merge(a, maps, sm, c, zero, first, count);
-      return;
-    }
-    for (; u < units; u += stride) {
-      combine_unit(a, u, tid & 31, first, zero ? 0 : count);
-      if (u + stride < units) combine_slots(a, u + stride, tid & 31, first, count);
-    }
+    tile_merge(a, maps, sm, c, c->merge_zero != 0, first, count);
   }
 }
 
