@@ -273,20 +273,35 @@ __device__ __forceinline__ int* ring_tile(uint8_t* sm, int t) {
 
 // Loader warp: tile j's 128 indices (invalid ones -> -1, flagged) into ring
 // slot j % NIDX, with the tile's first index and whether it is one run.  The
-// loads of four tiles are in flight together (the first tiles' latency is on
-// the critical path of the start).  (An L2 prefetch of the rows from this
-// warp measured slower: the prefetch instructions held the loader back.)
-__device__ void index_loader(const VerifyArgs& a, const Item& it, uint8_t* sm, Ctrl* c) {
-  constexpr int kBatch = 4;
+// loads of four tiles are in flight together, each at an address clamped into
+// the work item's keys (the keys past its end are masked when stored): a load
+// under a condition feeding a select would wait for each in turn.  The first
+// four tiles' loads are issued while the CTA is still being set up.  (An L2
+// prefetch of the rows from this warp measured slower: the prefetch
+// instructions held the loader back.)
+constexpr int kIdxBatch = 4;
+__device__ __forceinline__ void index_batch_load(const VerifyArgs& a, const Item& it, int j0, int lane,
+                                                 int (&v)[kIdxBatch][4]) {
+#pragma unroll
+  for (int jj = 0; jj < kIdxBatch; ++jj) {
+    const int k0 = it.k_begin + (j0 + jj) * TK + 4 * lane;
+#pragma unroll
+    for (int e = 0; e < 4; ++e) v[jj][e] = __ldg(a.kv_indices + it.loc.idx_base + min(k0 + e, it.k_end - 1));
+  }
+}
+__device__ void index_loader(const VerifyArgs& a, const Item& it, uint8_t* sm, Ctrl* c,
+                             const int (&first_batch)[kIdxBatch][4]) {
+  constexpr int kBatch = kIdxBatch;
   const int lane = threadIdx.x & 31;
   for (int j0 = 0; j0 < it.ntiles; j0 += kBatch) {
     int v[kBatch][4];
+    if (j0 == 0) {
 #pragma unroll
-    for (int jj = 0; jj < kBatch; ++jj) {
-      const int k0 = it.k_begin + (j0 + jj) * TK + 4 * lane;
+      for (int jj = 0; jj < kBatch; ++jj)
 #pragma unroll
-      for (int e = 0; e < 4; ++e)
-        v[jj][e] = (j0 + jj < it.ntiles && k0 + e < it.k_end) ? __ldg(a.kv_indices + it.loc.idx_base + k0 + e) : -1;
+        for (int e = 0; e < 4; ++e) v[jj][e] = first_batch[jj][e];
+    } else {
+      index_batch_load(a, it, j0, lane, v);
     }
 #pragma unroll
     for (int jj = 0; jj < kBatch; ++jj) {
@@ -297,7 +312,9 @@ __device__ void index_loader(const VerifyArgs& a, const Item& it, uint8_t* sm, C
       int* w = v[jj];
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
-        if (k0 + e < it.k_end && (w[e] < 0 || (a.pool_rows > 0 && w[e] >= a.pool_rows))) {
+        if (k0 + e >= it.k_end) {
+          w[e] = -1;  // past the work item's keys (the load was clamped)
+        } else if (w[e] < 0 || (a.pool_rows > 0 && w[e] >= a.pool_rows)) {
           atomicOr(a.status, DDTREE_ST_BAD_INDEX);
           w[e] = -1;
         }
@@ -400,7 +417,7 @@ __device__ __forceinline__ bool tma_count_in(const VerifyArgs& a, Ctrl* c, bool 
 
 // ------------------------------------------------------------------ scorer
 __device__ void scorer(const VerifyArgs& a, const PoolMaps& maps, const Item& it, uint8_t* sm, Ctrl* c,
-                       uint32_t rank, bool& joined) {
+                       uint32_t rank, bool& joined, const int (&first_idx)[kIdxBatch][4]) {
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const uint32_t tmem = c->tmem_base;  // [0,256): Q latent; [256,384), [384,512): S
   const bool leader = (rank & 1) == 0;
@@ -410,7 +427,7 @@ __device__ void scorer(const VerifyArgs& a, const PoolMaps& maps, const Item& it
   // (contiguous runs).  MMA issuers (leader): 1 (even tiles), 14 (odd).
   const int lsu = warp == 0 ? 0 : warp == 2 ? 1 : warp == 3 ? 2 : warp == 12 ? 3 : -1;
   if (warp == kLoaderWarp) {
-    index_loader(a, it, sm, c);
+    index_loader(a, it, sm, c, first_idx);
   } else if (lsu >= 0) {
     constexpr int G = 16 / kScLsuWarps;  // groups of four keys per warp (of the half's 16)
     uint32_t tpar = 0;                 // (warp 0) TMA phase parities, see tma_issuer
@@ -738,7 +755,7 @@ __device__ __forceinline__ bool rescaled(const uint8_t* sm, int s) {
 }
 
 __device__ void accumulator(const VerifyArgs& a, const PoolMaps& maps, const Item& it, uint8_t* sm, Ctrl* c,
-                            uint32_t rank, bool& joined) {
+                            uint32_t rank, bool& joined, const int (&first_idx)[kIdxBatch][4]) {
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const uint32_t tmem = c->tmem_base;  // O: cols [0,512)
   const bool leader = (rank & 1) == 0;
@@ -751,7 +768,7 @@ __device__ void accumulator(const VerifyArgs& a, const PoolMaps& maps, const Ite
                 : (warp >= 12 && warp <= 14) ? warp - 7 : -1;
 
   if (warp == kLoaderWarp) {
-    index_loader(a, it, sm, c);
+    index_loader(a, it, sm, c, first_idx);
   } else if (lsu >= 0) {
     constexpr int G = 32 / kAccLsuWarps;  // groups of four keys per warp (of the tile's 32)
     uint32_t tpar = 0;                 // (warp 0) TMA phase parities, see tma_issuer
@@ -941,8 +958,17 @@ __device__ void tile_merge(const VerifyArgs& a, const PoolMaps& maps, uint8_t* s
       const int row = r0 + warp;
       const bool live = row < a.rows_per_req;
       const float* pl = a.partial_lse + (size_t)first * a.rows_per_req + (live ? row : 0);
-      const float la = (live && lane < count) ? __ldcg(pl + (size_t)lane * a.rows_per_req) : -INFINITY;
-      const float lb = (live && lane + 32 < count) ? __ldcg(pl + (size_t)(lane + 32) * a.rows_per_req) : -INFINITY;
+      // Both loads issued together at clamped addresses and masked after (a
+      // load under a condition feeding a select would wait for each in
+      // turn); none when the request has no splits here (its first slot may
+      // then lie past the partials).
+      float xa = -INFINITY, xb = -INFINITY;
+      if (count > 0) {
+        xa = __ldcg(pl + (size_t)min(lane, count - 1) * a.rows_per_req);
+        xb = __ldcg(pl + (size_t)min(lane + 32, count - 1) * a.rows_per_req);
+      }
+      const float la = (live && lane < count) ? xa : -INFINITY;
+      const float lb = (live && lane + 32 < count) ? xb : -INFINITY;
       float m = fmaxf(la, lb);
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
@@ -1005,6 +1031,9 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(kThreads, 1)
   // still takes part in the cluster barriers and the pair's TMEM allocation.
 
   const bool work = have && it.ntiles > 0;
+  // The loader warp's first index loads, in flight during the set-up below.
+  int first_idx[kIdxBatch][4];
+  if (warp == kLoaderWarp && work) index_batch_load(a, it, 0, tid & 31, first_idx);
   if (tid == 0) {
     for (int i = 0; i < kMaxSlots; ++i) {
       mbar_init(&c->full[i], 32 * lsu_warps(rank) + 1);  // every load/store-unit lane, the TMA stream
@@ -1058,8 +1087,8 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(kThreads, 1)
   asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
   bool joined = false;
   if (work) {
-    if (rank < 2) scorer(a, maps, it, sm, c, rank, joined);
-    else accumulator(a, maps, it, sm, c, rank, joined);
+    if (rank < 2) scorer(a, maps, it, sm, c, rank, joined, first_idx);
+    else accumulator(a, maps, it, sm, c, rank, joined, first_idx);
   }
   join_cluster(joined);
   // The Q loads have landed before the CTA leaves (also after an expired wait).
