@@ -476,7 +476,7 @@ __device__ void scorer(const VerifyArgs& a, const PoolMaps& maps, const Item& it
   } else if (leader && (warp == 1 || warp == 14) && lane == 0) {
     // ---- MMA issuers for the pair, one per S buffer: warp 1 takes the even
     // tiles, warp 14 the odd ones, so one issuer's waits for its next tile
-    // overlap the other's MMAs.  Each tile once all of it landed.
+    // overlap the other's MMAs.  A tile goes out unit by unit as its units land.
     {
       constexpr uint32_t idesc = idesc_bf16_f32(256, 128, false, false);
       const uint64_t rope_desc = desc_sw128(smem_u32(sm + Q_ROPE), 16, 1024);
@@ -487,22 +487,17 @@ __device__ void scorer(const VerifyArgs& a, const PoolMaps& maps, const Item& it
       for (int t = s; t < it.ntiles && ok; t += 2) {
         const uint32_t sbuf = tmem + 256 + 128 * s;
         ok = wait_bar(&c->sempty[s], ((t >> 1) & 1) ^ 1, c, a.status);
-        // Only the tile's last unit is waited for, here and in the peer: each
-        // producer counts itself in on a unit only after its share of every
-        // earlier unit landed (cp.async arrivals fire once all of the lane's
-        // earlier copies completed; the TMA stream's count and the
-        // follower's forwards go unit by unit in order).
-        {
-          const int n = 3 * t + 2, slot = n % QSLOTS;
-          const uint32_t ph = (n / QSLOTS) & 1;
-          ok = ok && wait_bar(&c->full[slot], ph, c, a.status) && wait_bar(&c->peer[slot], ph, c, a.status);
-        }
-        if (!ok) break;
-        fence_async_smem();  // cp.async (generic proxy) data -> tensor-core reads
-        tc_fence_after();
+        // Each unit's MMAs go out as soon as it landed in both CTAs, so the
+        // tile's first units free their ring slots while its last one is
+        // still in flight (the ring's bytes in flight set the gather rate).
 #pragma unroll
-        for (int u = 0; u < 3; ++u) {
-          const int slot = (3 * t + u) % QSLOTS;
+        for (int u = 0; u < 3 && ok; ++u) {
+          const int n = 3 * t + u, slot = n % QSLOTS;
+          const uint32_t ph = (n / QSLOTS) & 1;
+          ok = wait_bar(&c->full[slot], ph, c, a.status) && wait_bar(&c->peer[slot], ph, c, a.status);
+          if (!ok) break;
+          fence_async_smem();  // cp.async (generic proxy) data -> tensor-core reads
+          tc_fence_after();
           const uint8_t* unit = sm + Q_RING + slot * QUNIT;
 #pragma unroll
           for (int cc = 0; cc < 3; ++cc) {  // chunk ch = 3u + cc: K steps 4ch .. 4ch+3 of the 36
@@ -513,6 +508,7 @@ __device__ void scorer(const VerifyArgs& a, const PoolMaps& maps, const Item& it
           }
           commit2(&c->empty[slot], kScorerPair);
         }
+        if (!ok) break;
         commit2(&c->sfull[s], kScorerPair);
       }
       commit2(&c->mma_done, kScorerPair);
