@@ -72,7 +72,11 @@ __device__ __forceinline__ int dev_prefix_len(const VerifyArgs& a, int b) {
 __device__ __forceinline__ bool locate_split(const VerifyArgs& a, int w, SplitLoc& loc) {
   int acc = 0;
   for (int r = 0; r < a.batch; ++r) {
+    // The request's index range is loaded together with its length (a load
+    // behind the length test would wait for the length first).
     int P = dev_prefix_len(a, r);
+    const auto i0 = a.kv_indptr ? __ldg(a.kv_indptr + r) : 0;
+    const auto i1 = a.kv_indptr ? __ldg(a.kv_indptr + r + 1) : 0;
     if (P < 0 || P > INT32_MAX - 2 * DDTREE_MAX_NODES) {
       atomicOr(a.status, DDTREE_ST_BAD_LENGTH);
       return false;
@@ -84,8 +88,8 @@ __device__ __forceinline__ bool locate_split(const VerifyArgs& a, int w, SplitLo
       loc.s = w - acc;
       loc.P = P;
       loc.nkeys = n;
-      loc.idx_base = a.kv_indptr ? (int64_t)__ldg(a.kv_indptr + r) : 0;
-      if (a.kv_indptr && __ldg(a.kv_indptr + r + 1) - __ldg(a.kv_indptr + r) != n) {
+      loc.idx_base = (int64_t)i0;
+      if (a.kv_indptr && i1 - i0 != n) {
         atomicOr(a.status, DDTREE_ST_BAD_LENGTH);
         return false;
       }

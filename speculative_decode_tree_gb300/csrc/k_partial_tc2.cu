@@ -135,6 +135,7 @@ struct __align__(8) Ctrl {
   uint32_t abort;
   float xmax[2][128];      // scorer: per-row maxima / sums exchanged between the softmax halves
   uint32_t merge_zero;     // fused merge: the partials cannot be trusted (a wait timed out)
+  uint32_t grid_arrived;   // fused merge: grid-barrier arrivals already made by the epilogue
   uint64_t anc[64];
   int32_t par[64];   // the request's parents, staged for the ancestor walk
 };
@@ -704,6 +705,7 @@ __device__ void acc_epilogue(const VerifyArgs& a, const PoolMaps& maps, const It
     const float l = c->xmax[0][r];
     const float inv = l > 0.f ? 1.f / l : 0.f;
     constexpr int kBox = ROWS * 128;  // 16 KB
+    const bool store = w == 0 && lane == 0 && it.row0 < a.rows_per_req;
 #pragma unroll 1
     for (int q = 4 * hc; q < 4 * hc + 4; ++q) {
       uint8_t* box = sm + V_RING + q * kBox;
@@ -724,18 +726,27 @@ __device__ void acc_epilogue(const VerifyArgs& a, const PoolMaps& maps, const It
               make_uint4(pk[0], pk[1], pk[2], pk[3]);
         }
       }
-    }
-    fence_async_smem();
-    named_bar(4 + hc, 128);
-    if (w == 0 && lane == 0 && it.row0 < a.rows_per_req) {
-      for (int q = 4 * hc; q < 4 * hc + 4; ++q)
+      // Each box goes out as soon as its 128 threads wrote it.
+      fence_async_smem();
+      named_bar(4 + hc, 128);
+      if (store) {
         asm volatile("cp.async.bulk.tensor.3d.global.shared::cta.tile.bulk_group [%0, {%1, %2, %3}], [%4];"
-                     ::"l"(&maps.po), "r"(64 * q), "r"(it.row0), "r"(it.slot), "r"(smem_u32(sm + V_RING + q * kBox))
+                     ::"l"(&maps.po), "r"(64 * q), "r"(it.row0), "r"(it.slot), "r"(smem_u32(box))
                      : "memory");
-      asm volatile("cp.async.bulk.commit_group;" ::: "memory");
-      asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
-      // The stores are read by other CTAs' ordinary loads in the fused merge.
-      asm volatile("fence.proxy.async;" ::: "memory");
+        asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+      }
+    }
+    if (w == 0 && lane == 0) {
+      if (store) {
+        asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+        // The stores are read by other CTAs in the fused merge.
+        asm volatile("fence.proxy.async;" ::: "memory");
+      }
+      // This half of the CTA's partial rows is in global memory: it counts
+      // itself in at the merge's grid barrier now (release), instead of after
+      // the CTA's teardown.  Both halves always do, so the CTA owes none later.
+      if (a.fused) asm volatile("red.release.gpu.global.add.u32 [%0], 1;" ::"l"(a.grid_done) : "memory");
+      if (hc == 0) c->grid_arrived = 2;
     }
   } else if (hc == 0 && it.row0 + r < a.rows_per_req) {
     for (int d = 0; d < kLatent; ++d)
@@ -988,14 +999,34 @@ __device__ void tile_merge(const VerifyArgs& a, const PoolMaps& maps, uint8_t* s
     if (row < a.rows_per_req) {
       const int h = col >> 8;
       const uint8_t* src = sm + h * box_bytes + rr * 512 + (col & 255) * 2;
-      float acc0 = 0.f, acc1 = 0.f;
-      if (ok)
-        for (int s = 0; s < count; ++s) {
-          const float w = wgt[64 * rr + s];
-          const uint32_t x = *reinterpret_cast<const uint32_t*>(src + (size_t)s * 1024);
-          acc0 = fmaf(w, bf16_lo(x), acc0);
-          acc1 = fmaf(w, bf16_hi(x), acc1);
+      // Four splits per step into two sums of each column (the loads of a
+      // step are independent; the chains are half as long).
+      float acc0 = 0.f, acc1 = 0.f, acc2 = 0.f, acc3 = 0.f;
+      if (ok) {
+        const float* wr = wgt + 64 * rr;
+        int s = 0;
+#pragma unroll 1
+        for (; s + 4 <= count; s += 4) {
+          uint32_t x[4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e) x[e] = *reinterpret_cast<const uint32_t*>(src + (size_t)(s + e) * 1024);
+          acc0 = fmaf(wr[s], bf16_lo(x[0]), acc0);
+          acc1 = fmaf(wr[s], bf16_hi(x[0]), acc1);
+          acc2 = fmaf(wr[s + 1], bf16_lo(x[1]), acc2);
+          acc3 = fmaf(wr[s + 1], bf16_hi(x[1]), acc3);
+          acc0 = fmaf(wr[s + 2], bf16_lo(x[2]), acc0);
+          acc1 = fmaf(wr[s + 2], bf16_hi(x[2]), acc1);
+          acc2 = fmaf(wr[s + 3], bf16_lo(x[3]), acc2);
+          acc3 = fmaf(wr[s + 3], bf16_hi(x[3]), acc3);
         }
+        for (; s < count; ++s) {
+          const uint32_t x = *reinterpret_cast<const uint32_t*>(src + (size_t)s * 1024);
+          acc0 = fmaf(wr[s], bf16_lo(x), acc0);
+          acc1 = fmaf(wr[s], bf16_hi(x), acc1);
+        }
+      }
+      acc0 += acc2;
+      acc1 += acc3;
       const size_t g = (size_t)b * a.rows_per_req + row;
       *reinterpret_cast<__nv_bfloat162*>(a.out + g * kLatent + col) = __floats2bfloat162_rn(acc0, acc1);
       if ((tid & 255) == 0) a.lse[g] = ok ? rowl[rr] : -INFINITY;
@@ -1056,6 +1087,7 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(kThreads, 1)
     mbar_init(&c->qload, 1);
     mbar_init(&c->mload, 1);
     c->abort = 0;
+    c->grid_arrived = 0;
     c->wait_ns = a.wait_ns;
     fence_mbar_init();
     if (rank < 2 && work) {
@@ -1092,6 +1124,16 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(kThreads, 1)
 
   tc_fence_before();
   __syncthreads();
+  if (a.fused && tid == 0) {
+    // Fused merge: every CTA counts 2 at the grid barrier.  An accumulator's
+    // epilogue did so as soon as its partial rows were stored; the rest
+    // count here, as soon as the CTA's own writes (LSEs, zero rows) are done,
+    // without waiting for the rest of the cluster.  Release: those writes,
+    // ordered before this thread by the barrier above, are visible to
+    // whoever sees the count.
+    const uint32_t late = 2u - c->grid_arrived;
+    if (late) asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(a.grid_done), "r"(late) : "memory");
+  }
   // Tensor-core work writing this CTA's TMEM must be finished before it is freed.
   if (warp == 3 && work) mbar_wait_cluster(&c->mma_done, 0, kDrainNs);
   tc_fence_before();
@@ -1103,24 +1145,20 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(kThreads, 1)
 
   if (a.fused) {
     // Merge the splits in this launch: every CTA of the grid is resident at
-    // once (cooperative launch), so each counts itself done and waits,
-    // bounded, for all others; then each CTA merges two rows at a time from
-    // one tile load of all their splits (the plan fuses only when a
-    // request's splits fit it).  A timed-out wait anywhere writes zeros.
-    // The split range of the CTA's first unit is looked up while the grid
-    // finishes.
+    // once (cooperative launch), so each, having counted itself in above,
+    // waits, bounded, for all others; then each CTA merges two rows at a
+    // time from one tile load of all their splits (the plan fuses only when
+    // a request's splits fit it).  A timed-out wait anywhere writes zeros.
+    // The split range of the CTA's first unit, looked up while the grid finishes.
     int first = 0, count = 0;
     if ((int)blockIdx.x < tile_merge_units(a)) tile_merge_slots(a, blockIdx.x, first, count);
     if (tid == 0) {
-      // Release: this CTA's partials (stored before the cluster barrier
-      // above) are visible to whoever sees the count.
-      asm volatile("red.release.gpu.global.add.u32 [%0], 1;" ::"l"(a.grid_done) : "memory");
       uint64_t deadline = 0;
       bool ok = true;
       for (uint32_t spin = 1;; ++spin) {
         uint32_t v;
         asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(a.grid_done) : "memory");
-        if (v >= gridDim.x) break;
+        if (v >= 2u * gridDim.x) break;
         if (spin == 4u) {
           deadline = global_timer_ns() + a.wait_ns;
         } else if (spin > 4u && (spin & 7u) == 0u && global_timer_ns() > deadline) {
