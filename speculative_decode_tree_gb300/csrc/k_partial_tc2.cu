@@ -133,7 +133,7 @@ struct __align__(8) Ctrl {
   uint64_t wait_ns;        // bound of the waits (the caller's, default 2 s)
   uint32_t tmem_base;
   uint32_t abort;
-  float xmax[2][128];      // scorer: per-row maxima / sums exchanged between the softmax halves
+  alignas(16) float xmax[2][128];  // scorer: per-row maxima / sums exchanged between the softmax halves
   uint32_t merge_zero;     // fused merge: the partials cannot be trusted (a wait timed out)
   uint32_t grid_arrived;   // fused merge: grid-barrier arrivals already made by the epilogue
   uint64_t anc[64];
@@ -685,6 +685,16 @@ __device__ void scorer(const VerifyArgs& a, const PoolMaps& maps, const Item& it
   }
 }
 
+// Count n arrivals at the fused merge's grid barrier (every CTA counts 2).
+// Release: the caller's writes (and what it has seen) are visible to whoever
+// sees the count complete.  The arrival that completes it raises the flag the
+// other CTAs poll, which lives in its own line, apart from the atomics.
+__device__ __forceinline__ void grid_arrive(const VerifyArgs& a, uint32_t n) {
+  uint32_t old;
+  asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], %2;" : "=r"(old) : "l"(a.grid_done), "r"(n) : "memory");
+  if (old + n == 2u * gridDim.x) asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(a.grid_go), "r"(1u) : "memory");
+}
+
 // ------------------------------------------------------------ accumulator
 // Accumulator epilogue: O_s = O / l as bf16 rows of the workspace, by eight
 // warps -- 4..7 (after the tile loop) write columns 0..255, 12..15 columns
@@ -745,7 +755,7 @@ __device__ void acc_epilogue(const VerifyArgs& a, const PoolMaps& maps, const It
       // This half of the CTA's partial rows is in global memory: it counts
       // itself in at the merge's grid barrier now (release), instead of after
       // the CTA's teardown.  Both halves always do, so the CTA owes none later.
-      if (a.fused) asm volatile("red.release.gpu.global.add.u32 [%0], 1;" ::"l"(a.grid_done) : "memory");
+      if (a.fused) grid_arrive(a, 1);
       if (hc == 0) c->grid_arrived = 2;
     }
   } else if (hc == 0 && it.row0 + r < a.rows_per_req) {
@@ -1007,17 +1017,18 @@ __device__ void tile_merge(const VerifyArgs& a, const PoolMaps& maps, uint8_t* s
         int s = 0;
 #pragma unroll 1
         for (; s + 4 <= count; s += 4) {
+          const float4 w = *reinterpret_cast<const float4*>(wr + s);  // one load for four weights
           uint32_t x[4];
 #pragma unroll
           for (int e = 0; e < 4; ++e) x[e] = *reinterpret_cast<const uint32_t*>(src + (size_t)(s + e) * 1024);
-          acc0 = fmaf(wr[s], bf16_lo(x[0]), acc0);
-          acc1 = fmaf(wr[s], bf16_hi(x[0]), acc1);
-          acc2 = fmaf(wr[s + 1], bf16_lo(x[1]), acc2);
-          acc3 = fmaf(wr[s + 1], bf16_hi(x[1]), acc3);
-          acc0 = fmaf(wr[s + 2], bf16_lo(x[2]), acc0);
-          acc1 = fmaf(wr[s + 2], bf16_hi(x[2]), acc1);
-          acc2 = fmaf(wr[s + 3], bf16_lo(x[3]), acc2);
-          acc3 = fmaf(wr[s + 3], bf16_hi(x[3]), acc3);
+          acc0 = fmaf(w.x, bf16_lo(x[0]), acc0);
+          acc1 = fmaf(w.x, bf16_hi(x[0]), acc1);
+          acc2 = fmaf(w.y, bf16_lo(x[1]), acc2);
+          acc3 = fmaf(w.y, bf16_hi(x[1]), acc3);
+          acc0 = fmaf(w.z, bf16_lo(x[2]), acc0);
+          acc1 = fmaf(w.z, bf16_hi(x[2]), acc1);
+          acc2 = fmaf(w.w, bf16_lo(x[3]), acc2);
+          acc3 = fmaf(w.w, bf16_hi(x[3]), acc3);
         }
         for (; s < count; ++s) {
           const uint32_t x = *reinterpret_cast<const uint32_t*>(src + (size_t)s * 1024);
@@ -1132,7 +1143,7 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(kThreads, 1)
     // ordered before this thread by the barrier above, are visible to
     // whoever sees the count.
     const uint32_t late = 2u - c->grid_arrived;
-    if (late) asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(a.grid_done), "r"(late) : "memory");
+    if (late) grid_arrive(a, late);
   }
   // Tensor-core work writing this CTA's TMEM must be finished before it is freed.
   if (warp == 3 && work) mbar_wait_cluster(&c->mma_done, 0, kDrainNs);
@@ -1155,10 +1166,12 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(kThreads, 1)
     if (tid == 0) {
       uint64_t deadline = 0;
       bool ok = true;
+      // Relaxed polls of the flag the last arrival raises; one acquire fence
+      // once it is seen.
       for (uint32_t spin = 1;; ++spin) {
         uint32_t v;
-        asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(a.grid_done) : "memory");
-        if (v >= 2u * gridDim.x) break;
+        asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(a.grid_go) : "memory");
+        if (v != 0u) break;
         if (spin == 4u) {
           deadline = global_timer_ns() + a.wait_ns;
         } else if (spin > 4u && (spin & 7u) == 0u && global_timer_ns() > deadline) {
@@ -1166,9 +1179,10 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(kThreads, 1)
           break;
         }
       }
+      asm volatile("fence.acq_rel.gpu;" ::: "memory");
       if (!ok) atomicOr(a.status, DDTREE_ST_TIMEOUT);
       uint32_t st;
-      asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(st) : "l"(a.status) : "memory");
+      asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(st) : "l"(a.status) : "memory");
       c->merge_zero = (!ok || (st & DDTREE_ST_TIMEOUT)) ? 1u : 0u;
     }
     __syncthreads();

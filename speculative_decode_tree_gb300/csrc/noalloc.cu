@@ -13,8 +13,9 @@
 // The scratch is a file-scope device array of DDTREE_NOALLOC_SCRATCH_BYTES
 // (8 MiB).  Every GPU that loads this library keeps those bytes reserved
 // until the process exits.  All calls on a device share the one array and it
-// keeps whatever the previous call left there: the status word at its start
-// is cleared on the stream at the beginning of every call, and every partial
+// keeps whatever the previous call left there: the status block at its start
+// (status word and merge counters, 256 bytes) is cleared on the stream at the
+// beginning of every call, and every partial
 // result a call reads is written earlier in the same call.  Two calls whose
 // work overlaps on the GPU (different streams, or different host threads)
 // race on the array and corrupt each other's results; serialise them.
@@ -130,6 +131,7 @@ extern "C" int ddtree_verify_mla_noalloc(const ddtree_bf16_t* q_latent, const dd
   uint8_t* ws = static_cast<uint8_t*>(scratch);
   a.status = reinterpret_cast<uint32_t*>(ws);
   a.grid_done = reinterpret_cast<uint32_t*>(ws + 8);
+  a.grid_go = reinterpret_cast<uint32_t*>(ws + 128);  // its own 128-byte line
   a.partial_lse = reinterpret_cast<float*>(ws + plan.off_partial_lse);
   a.partial_o = reinterpret_cast<uint16_t*>(ws + plan.off_partial_o);
   a.fused = plan.fused_combine;
@@ -150,7 +152,7 @@ extern "C" int ddtree_verify_mla_noalloc(const ddtree_bf16_t* q_latent, const dd
   a.q_rope_stride = kRope;
 
   cudaStream_t s = (cudaStream_t)stream;
-  if (cudaMemsetAsync(a.status, 0, 16, s) != cudaSuccess) {
+  if (cudaMemsetAsync(a.status, 0, 256, s) != cudaSuccess) {
     cudaGetLastError();
     return DDTREE_ECUDA;
   }
