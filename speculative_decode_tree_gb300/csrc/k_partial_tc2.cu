@@ -129,7 +129,7 @@ struct __align__(8) Ctrl {
   uint64_t mma_done;
   uint64_t q_ready;   // scorer: Q latent in TMEM and Q rope in shared memory
   uint64_t qload;     // scorer: the TMA loads of Q (latent staging + rope) landed
-  uint64_t mload;     // fused merge: a unit's partials landed
+  uint64_t mload[2];  // fused merge: column half h of a unit's partials landed
   uint64_t wait_ns;        // bound of the waits (the caller's, default 2 s)
   uint32_t tmem_base;
   uint32_t abort;
@@ -964,12 +964,13 @@ __device__ void tile_merge(const VerifyArgs& a, const PoolMaps& maps, uint8_t* s
       // The partials were written by other CTAs' TMA stores, seen through
       // the grid barrier (generic proxy); these loads are async proxy.
       asm volatile("fence.proxy.async.global;" ::: "memory");
-      mbar_arrive_expect_tx(&c->mload, 2 * box_bytes);
-      for (int h = 0; h < 2; ++h)
+      for (int h = 0; h < 2; ++h) {
+        mbar_arrive_expect_tx(&c->mload[h], box_bytes);
         asm volatile(
             "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], [%5];"
-            ::"r"(smem_u32(sm + h * box_bytes)), "l"(&maps.pm), "r"(256 * h), "r"(r0), "r"(first), "r"(smem_u32(&c->mload))
+            ::"r"(smem_u32(sm + h * box_bytes)), "l"(&maps.pm), "r"(256 * h), "r"(r0), "r"(first), "r"(smem_u32(&c->mload[h]))
             : "memory");
+      }
     }
     if (warp < 2) {  // warp w: the weights of row r0 + w (lane j: splits j, j + 32)
       const int row = r0 + warp;
@@ -1000,38 +1001,40 @@ __device__ void tile_merge(const VerifyArgs& a, const PoolMaps& maps, uint8_t* s
       if (lane == 0) rowl[warp] = l > 0.f ? m + logf(l) : -INFINITY;
     }
     __syncthreads();
-    bool ok = true;
-    if (count > 0) ok = mbar_wait(&c->mload, ph, a.wait_ns);
-    if (!ok && tid == 0) atomicOr(a.status, DDTREE_ST_TIMEOUT);
-    // thread: row r0 + (tid >> 8), columns 2 (tid & 255) .. + 1
+    // thread: row r0 + (tid >> 8), columns 2 (tid & 255) .. + 1, of column
+    // half h (uniform in a warp); it waits only for its half's box.
     const int rr = tid >> 8, col = 2 * (tid & 255);
     const int row = r0 + rr;
+    const int h = col >> 8;
+    bool ok = true;
+    if (count > 0) ok = mbar_wait(&c->mload[h], ph, a.wait_ns);
+    if (!ok && lane == 0) atomicOr(a.status, DDTREE_ST_TIMEOUT);
     if (row < a.rows_per_req) {
-      const int h = col >> 8;
-      const uint8_t* src = sm + h * box_bytes + rr * 512 + (col & 255) * 2;
-      // Four splits per step into two sums of each column (the loads of a
-      // step are independent; the chains are half as long).
+      const uint8_t* src = sm + h * box_bytes + rr * 512 + (col & 255) * 2;  // split s at + 1 KB s
+      // Eight splits per step (eight independent loads, two 16-byte weight
+      // loads) into two sums of each column.
       float acc0 = 0.f, acc1 = 0.f, acc2 = 0.f, acc3 = 0.f;
       if (ok) {
         const float* wr = wgt + 64 * rr;
         int s = 0;
 #pragma unroll 1
-        for (; s + 4 <= count; s += 4) {
-          const float4 w = *reinterpret_cast<const float4*>(wr + s);  // one load for four weights
-          uint32_t x[4];
+        for (; s + 8 <= count; s += 8) {
+          const float4 wa = *reinterpret_cast<const float4*>(wr + s);
+          const float4 wb = *reinterpret_cast<const float4*>(wr + s + 4);
+          const float w[8] = {wa.x, wa.y, wa.z, wa.w, wb.x, wb.y, wb.z, wb.w};
+          uint32_t x[8];
 #pragma unroll
-          for (int e = 0; e < 4; ++e) x[e] = *reinterpret_cast<const uint32_t*>(src + (size_t)(s + e) * 1024);
-          acc0 = fmaf(w.x, bf16_lo(x[0]), acc0);
-          acc1 = fmaf(w.x, bf16_hi(x[0]), acc1);
-          acc2 = fmaf(w.y, bf16_lo(x[1]), acc2);
-          acc3 = fmaf(w.y, bf16_hi(x[1]), acc3);
-          acc0 = fmaf(w.z, bf16_lo(x[2]), acc0);
-          acc1 = fmaf(w.z, bf16_hi(x[2]), acc1);
-          acc2 = fmaf(w.w, bf16_lo(x[3]), acc2);
-          acc3 = fmaf(w.w, bf16_hi(x[3]), acc3);
+          for (int e = 0; e < 8; ++e) x[e] = *reinterpret_cast<const uint32_t*>(src + (s + e) * 1024);
+#pragma unroll
+          for (int e = 0; e < 8; e += 2) {
+            acc0 = fmaf(w[e], bf16_lo(x[e]), acc0);
+            acc1 = fmaf(w[e], bf16_hi(x[e]), acc1);
+            acc2 = fmaf(w[e + 1], bf16_lo(x[e + 1]), acc2);
+            acc3 = fmaf(w[e + 1], bf16_hi(x[e + 1]), acc3);
+          }
         }
         for (; s < count; ++s) {
-          const uint32_t x = *reinterpret_cast<const uint32_t*>(src + (size_t)s * 1024);
+          const uint32_t x = *reinterpret_cast<const uint32_t*>(src + s * 1024);
           acc0 = fmaf(wr[s], bf16_lo(x), acc0);
           acc1 = fmaf(wr[s], bf16_hi(x), acc1);
         }
@@ -1096,7 +1099,7 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(kThreads, 1)
     mbar_init(&c->mma_done, 2);  // two MMA issuers per pair
     mbar_init(&c->q_ready, 8);
     mbar_init(&c->qload, 1);
-    mbar_init(&c->mload, 1);
+    for (int i = 0; i < 2; ++i) mbar_init(&c->mload[i], 1);
     c->abort = 0;
     c->grid_arrived = 0;
     c->wait_ns = a.wait_ns;
