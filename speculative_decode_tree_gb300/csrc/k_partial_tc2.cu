@@ -31,14 +31,23 @@
 // 16-byte cp.async (measured faster per SM than TMA gather4 for these rows);
 // a tile whose 128 indices form one contiguous run comes by 2-D TMA tile
 // loads instead.  TMA loads complete on the stream's own barriers (one warp
-// issues, a second warp waits for each unit's bytes and then counts the
-// stream in), so every load a CTA issued is known to have landed before it
-// exits, also after an expired wait.  No warp runs two spinning roles: a lane
-// suspended in a barrier wait holds back every other lane of its warp.  The scorer's key ring holds seven units of
-// three chunks (2.3 tiles), enough to keep the next tile's rows in flight
-// while a tile is multiplied.  The follower CTA of each pair forwards "my
-// unit is complete" to the leader, whose MMA thread waits for a whole tile
-// and then issues its MMAs back to back.
+// issues; a lane of a load/store-unit warp waits for each unit's bytes and
+// counts the stream in), so every load a CTA issued is known to have landed
+// before it exits, also after an expired wait.  No warp runs two spinning
+// roles: a lane suspended in a barrier wait holds back every other lane of
+// its warp.  The scorer's key ring holds seven units of three chunks (2.3
+// tiles), enough to keep the next tile's rows in flight while a tile is
+// multiplied.  The follower CTA of each pair forwards "my unit is complete"
+// to the leader, whose MMA threads (one per S buffer) issue each unit's MMAs
+// as soon as the unit is complete in both CTAs.
+//
+// Merge ("Chunk 66.0": partial + reduce): with a one-wave plan the launch is
+// cooperative and the kernel merges its own splits.  Each CTA counts 2 at a
+// grid barrier as soon as its own writes are done (an accumulator's two
+// epilogue store threads once their TMA stores complete; every other CTA
+// before the cluster teardown); the arrival that completes the count raises
+// a flag in a line of its own, which every CTA polls.  Then each CTA merges
+// two rows of a request from TMA tile loads of all their splits.
 //
 // Every mbarrier wait is bounded; on expiry the kernel sets
 // DDTREE_ST_TIMEOUT, stops issuing work, waits (bounded) for its own
