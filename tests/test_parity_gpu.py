@@ -54,6 +54,44 @@ def test_small_shapes_match_oracle(shape, kernel):
     _compare_all(inp, kernel, f"P={P} T={T} H={H}")
 
 
+def _random_shapes(n: int, seed: int):
+    """Seeded draws of (batch, T, H, prefixes, tree, index mode): plans of
+    every kind the library picks by default (split counts, fused merge or
+    not, one or two row tiles, empty and one-key prefixes)."""
+    import random
+    r = random.Random(seed)
+    shapes = []
+    for _ in range(n):
+        batch = r.randint(1, 4)
+        T = r.choice([1, 3, 8, 16, 31, 32, 48, 64])
+        H = r.choice([1, 2, 4, 8, 16])
+        while T * H > 512:
+            H //= 2
+        prefixes = [r.choice([0, 1, r.randint(2, 300), r.randint(300, 4000)]) for _ in range(batch)]
+        shapes.append((batch, T, H, prefixes, r.choice(["chain", "uniform", "bounded"]),
+                       r.choice(["sample", "interleaved"])))
+    return shapes
+
+
+RANDOM = _random_shapes(12, seed=20261203) + [
+    # longer prefixes: several splits per request, fused merge over many of them
+    (2, 16, 8, [20000, 9000], "uniform", "interleaved"),
+    (1, 32, 8, [30000], "bounded", "sample"),
+]
+
+
+@pytest.mark.parametrize("kernel", [None, B.DDTREE_KERNEL_TC2], ids=["auto", "tc2"])
+@pytest.mark.parametrize("shape", RANDOM, ids=[f"B{s[0]}_T{s[1]}_H{s[2]}_{s[4]}_{s[5]}" for s in RANDOM])
+def test_random_plans_match_oracle(shape, kernel):
+    batch, T, H, prefixes, tree, mode = shape
+    pool_rows = max(1024, 2 * sum(p + T for p in prefixes))
+    inp = make_inputs("random", batch=batch, n_heads=H, prefixes=prefixes, n_nodes=T, tree=tree,
+                      pool_rows=pool_rows, index_mode=mode, seed=batch + 3 * T + 11 * H + sum(prefixes))
+    dv = _compare_all(inp, kernel, f"B={batch} T={T} H={H} P={prefixes} {tree} {mode}")
+    if kernel is not None:
+        assert dv.plan.kernel == kernel
+
+
 @pytest.mark.parametrize("kernel", KERNELS)
 def test_ragged_batch_matches_oracle(kernel):
     prefixes = [0, 5, 777, 64, 1, 2049, 31, 300]
