@@ -390,7 +390,8 @@ def run_ours(args, world, rank, local):
     # inputs (queries, indices, parents, lengths) and D2H of out + lse.  The
     # inputs sit in one pinned host arena and one device arena (one H2D copy),
     # out and lse side by side in one device arena (one D2H copy); the call
-    # takes views into the arenas.
+    # takes views into the arenas, bound once (the buffers stay the same from
+    # step to step, as in a decode loop).
     e2e = None
     if not args.no_e2e:
         src = (inp.q_latent, inp.q_rope, inp.kv_indices, inp.kv_indptr, inp.prefix_lens, inp.tree_parent)
@@ -403,14 +404,15 @@ def run_ours(args, world, rank, local):
         h2d = host_in.numel()
         d2h = host_out.numel()
         q_lat, q_rope, kv_idx, kv_ptr, p_lens, t_par = d_views
+        call = B.BoundVerify(dv.plan, q_lat, q_rope, dv.kv_pool, kv_idx, kv_ptr, p_lens, t_par, inp.sm_scale,
+                             out_v, lse_v, dv.workspace)
         es = []
         for i in range(args.warmup + args.steps):
             with torch.cuda.stream(stream):
                 flush.zero_()
                 t0.record(stream)
                 dev_in.copy_(host_in, non_blocking=True)
-                B.ddtree_verify_mla_batched(dv.plan, q_lat, q_rope, dv.kv_pool, kv_idx, kv_ptr, p_lens, t_par,
-                                            inp.sm_scale, out_v, lse_v, dv.workspace, stream)
+                call(stream)
                 host_out.copy_(dev_out, non_blocking=True)
                 t1.record(stream)
             stream.synchronize()

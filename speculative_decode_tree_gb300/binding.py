@@ -121,18 +121,20 @@ def _ptr(t: Optional[torch.Tensor]) -> Optional[int]:
 
 
 def _dev(t: torch.Tensor, dtype: torch.dtype, name: str, numel: Optional[int] = None,
-         contiguous: bool = True) -> int:
+         contiguous: bool = True, device: Optional[int] = None) -> int:
     """Device pointer of `t` after checking what the kernels rely on: a CUDA
-    tensor of `dtype` on the current device, contiguous (unless the caller
-    checks its layout), holding at least `numel` elements.  The C ABI trusts
-    the sizes it derives itself, so an undersized or foreign buffer is
-    rejected here, before any launch."""
+    tensor of `dtype` on the current device (`device`, when the caller looked
+    it up once for several tensors), contiguous (unless the caller checks its
+    layout), holding at least `numel` elements.  The C ABI trusts the sizes it
+    derives itself, so an undersized or foreign buffer is rejected here,
+    before any launch."""
     if not isinstance(t, torch.Tensor) or not t.is_cuda:
         raise TypeError(f"{name} must be a CUDA tensor")
     if t.dtype != dtype:
         raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
-    if t.device.index != torch.cuda.current_device():
-        raise ValueError(f"{name} is on {t.device}, not the current device cuda:{torch.cuda.current_device()}")
+    cur = torch.cuda.current_device() if device is None else device
+    if t.get_device() != cur:
+        raise ValueError(f"{name} is on {t.device}, not the current device cuda:{cur}")
     if contiguous and not t.is_contiguous():
         raise ValueError(f"{name} must be contiguous")
     if numel is not None and t.numel() < numel:
@@ -140,19 +142,20 @@ def _dev(t: torch.Tensor, dtype: torch.dtype, name: str, numel: Optional[int] = 
     return t.data_ptr()
 
 
-def _q(t: torch.Tensor, name: str, rows: int, width: int, row_stride: int) -> int:
+def _q(t: torch.Tensor, name: str, rows: int, width: int, row_stride: int, device: Optional[int] = None) -> int:
     """Pointer of a query operand: `rows` rows of `width` bf16 values whose
     starts are `row_stride` elements apart (width when 0), e.g. views
     q[..., :512] and q[..., 512:] of one [tokens, heads, 576] tensor."""
     stride = row_stride or width
-    _dev(t, torch.bfloat16, name, contiguous=False)
-    if t.dim() < 2 or t.shape[-1] != width or t.stride(-1) != 1 or t.numel() != rows * width:
+    _dev(t, torch.bfloat16, name, contiguous=False, device=device)
+    shape, strides = t.shape, t.stride()
+    if len(shape) < 2 or shape[-1] != width or strides[-1] != 1 or t.numel() != rows * width:
         raise ValueError(f"{name} must be [..., {width}] with {rows} rows of unit-stride elements")
     expect = stride
-    for d in range(t.dim() - 2, -1, -1):  # every leading dimension steps whole rows
-        if t.shape[d] > 1 and t.stride(d) != expect:
+    for d in range(len(shape) - 2, -1, -1):  # every leading dimension steps whole rows
+        if shape[d] > 1 and strides[d] != expect:
             raise ValueError(f"{name}: row stride must be {stride} elements (plan q_*_row_stride)")
-        expect *= t.shape[d]
+        expect *= shape[d]
     return t.data_ptr()
 
 
@@ -233,12 +236,15 @@ def _batched_args(plan: Plan, q_latent, q_rope, kv_pool, kv_indices, kv_indptr, 
     bf, i32 = torch.bfloat16, torch.int32
     b, t, rows = plan.batch, plan.n_nodes, plan.batch * plan.rows_per_req
     pool_numel = plan.pool_rows * 576 if plan.pool_rows > 0 else None
-    return (ctypes.byref(plan), _q(q_latent, "q_latent", rows, 512, plan.q_latent_row_stride),
-            _q(q_rope, "q_rope", rows, 64, plan.q_rope_row_stride), _dev(kv_pool, bf, "kv_pool", pool_numel),
-            _dev(kv_indices, i32, "kv_indices"), _dev(kv_indptr, i32, "kv_indptr", b + 1),
-            _dev(prefix_lens, i32, "prefix_lens", b), _dev(tree_parent, i32, "tree_parent", b * t),
-            float(sm_scale), _dev(out, bf, "out", rows * 512), _dev(lse, torch.float32, "lse", rows),
-            _dev(workspace, torch.uint8, "workspace", plan.workspace_bytes), workspace.numel())
+    ql = _q(q_latent, "q_latent", rows, 512, plan.q_latent_row_stride)  # a CUDA tensor on the current device
+    d = q_latent.get_device()  # so the current device, for the call's other tensors
+    return (ctypes.byref(plan), ql,
+            _q(q_rope, "q_rope", rows, 64, plan.q_rope_row_stride, d),
+            _dev(kv_pool, bf, "kv_pool", pool_numel, device=d),
+            _dev(kv_indices, i32, "kv_indices", device=d), _dev(kv_indptr, i32, "kv_indptr", b + 1, device=d),
+            _dev(prefix_lens, i32, "prefix_lens", b, device=d), _dev(tree_parent, i32, "tree_parent", b * t, device=d),
+            float(sm_scale), _dev(out, bf, "out", rows * 512, device=d), _dev(lse, torch.float32, "lse", rows, device=d),
+            _dev(workspace, torch.uint8, "workspace", plan.workspace_bytes, device=d), workspace.numel())
 
 
 def ddtree_verify_mla_batched(plan: Plan, q_latent, q_rope, kv_pool, kv_indices, kv_indptr,
@@ -248,6 +254,25 @@ def ddtree_verify_mla_batched(plan: Plan, q_latent, q_rope, kv_pool, kv_indices,
         *_batched_args(plan, q_latent, q_rope, kv_pool, kv_indices, kv_indptr, prefix_lens, tree_parent,
                        sm_scale, out, lse, workspace), _stream(stream))
     _check(rc, "ddtree_verify_mla_batched")
+
+
+class BoundVerify:
+    """ddtree_verify_mla_batched with its arguments checked and marshalled
+    once, for callers whose buffers stay the same from call to call (a decode
+    loop with static buffers).  Calling the object launches the verify on
+    `stream`.  It keeps references to the plan and tensors; they must not be
+    resized or moved in place (`resize_`, `set_`) while the object is used."""
+
+    def __init__(self, plan: Plan, q_latent, q_rope, kv_pool, kv_indices, kv_indptr, prefix_lens,
+                 tree_parent, sm_scale: float, out, lse, workspace):
+        self._keep = (plan, q_latent, q_rope, kv_pool, kv_indices, kv_indptr, prefix_lens, tree_parent,
+                      out, lse, workspace)
+        self._args = _batched_args(plan, q_latent, q_rope, kv_pool, kv_indices, kv_indptr, prefix_lens,
+                                   tree_parent, sm_scale, out, lse, workspace)
+        self._fn = library().ddtree_verify_mla_batched
+
+    def __call__(self, stream=None) -> None:
+        _check(self._fn(*self._args, _stream(stream)), "ddtree_verify_mla_batched")
 
 
 def ddtree_verify_mla_batched_timed(plan: Plan, q_latent, q_rope, kv_pool, kv_indices, kv_indptr,

@@ -322,3 +322,35 @@ def test_graph_replay_batched_with_changing_lengths(kernel):
             O_ref, L_ref = oracle_rows(new, b)
             assert_within_tolerance(dv.out[b * T:(b + 1) * T], dv.lse[b * T:(b + 1) * T], O_ref, L_ref,
                                     f"replay {prefixes} request {b}")
+
+
+def test_bound_call_matches_the_batched_call_and_sees_new_inputs_in_place():
+    """BoundVerify marshals its buffers once; each call reads their current
+    contents (new queries written in place between calls)."""
+    inp = make_inputs("bound", batch=2, n_heads=8, prefixes=[3000, 700], n_nodes=16, tree="uniform",
+                      pool_rows=8192, index_mode="interleaved", seed=5)
+    dv = DeviceVerify(inp)
+    dv.run()
+    ref_out, ref_lse = dv.out.clone(), dv.lse.clone()
+    out, lse = torch.empty_like(dv.out), torch.empty_like(dv.lse)
+    call = B.BoundVerify(dv.plan, dv.q_latent, dv.q_rope, dv.kv_pool, dv.kv_indices, dv.kv_indptr, dv.prefix_lens,
+                         dv.tree_parent, inp.sm_scale, out, lse, dv.workspace)
+    call()
+    torch.cuda.synchronize()
+    assert torch.equal(out, ref_out) and torch.equal(lse, ref_lse)
+    # New queries in the same buffers: the bound call computes with them.
+    other = make_inputs("bound2", batch=2, n_heads=8, prefixes=[3000, 700], n_nodes=16, tree="uniform",
+                        pool_rows=8192, index_mode="interleaved", seed=6)
+    dv.q_latent.copy_(other.q_latent)
+    dv.q_rope.copy_(other.q_rope)
+    call()
+    torch.cuda.synchronize()
+    assert dv.status() == 0
+    from oracle import verify_request
+    T = inp.n_nodes
+    for b in range(inp.batch):
+        lo, hi = int(inp.kv_indptr[b]), int(inp.kv_indptr[b + 1])
+        O_ref, L_ref = verify_request(other.q_latent[b * T:(b + 1) * T], other.q_rope[b * T:(b + 1) * T],
+                                      inp.kv_pool, inp.kv_indices[lo:hi], int(inp.prefix_lens[b]),
+                                      inp.tree_parent[b].tolist(), inp.sm_scale)
+        assert_within_tolerance(out[b * T:(b + 1) * T], lse[b * T:(b + 1) * T], O_ref, L_ref, f"bound request {b}")
