@@ -59,6 +59,7 @@ struct SplitLoc {
   int s;            // split within the request
   int P;            // prefix length
   int nkeys;        // P + T
+  int ns;           // splits of the request
   int64_t idx_base; // first kv_indices entry of the request
 };
 
@@ -89,6 +90,7 @@ __device__ __forceinline__ bool locate_split(const VerifyArgs& a, int w, SplitLo
       loc.s = w - acc;
       loc.P = P;
       loc.nkeys = n;
+      loc.ns = ns;
       loc.idx_base = (int64_t)i0;
       if (a.kv_indptr && i1 - i0 != n) {
         atomicOr(a.status, DDTREE_ST_BAD_LENGTH);

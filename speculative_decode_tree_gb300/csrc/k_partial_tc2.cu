@@ -252,6 +252,7 @@ struct Item {
   int k_end;     // one past the last key
   int ntiles;
   int slot;      // split slot in the workspace
+  bool direct;   // the request's only split, merged in this launch: final rows, no partials
 };
 
 struct PoolMaps {
@@ -261,6 +262,7 @@ struct PoolMaps {
   CUtensorMap ql;     // Q latent [B*T*H rows][512] bf16, 64 columns x 128 rows box
   CUtensorMap qr;     // Q rope [B*T*H rows][64] bf16, 64 columns x 128 rows box
   CUtensorMap pm;     // partial O again, unswizzled box of 256 columns x 2 rows x merge_depth splits
+  CUtensorMap fo;     // out as [batch][rows_per_req][512]: single-split requests' final rows
 };
 
 // The start-of-kernel cluster barrier is split: every thread arrives once its
@@ -687,8 +689,9 @@ __device__ void scorer(const VerifyArgs& a, const PoolMaps& maps, const Item& it
     named_bar(1, 256);
     if (hw == 0 && row_ok) {
       const float lt = l + c->xmax[1][r];
-      a.partial_lse[(size_t)it.slot * a.rows_per_req + req_row] =
-          (lt > 0.f) ? (m_ref + log2f(lt)) * 0.6931471805599453f : -INFINITY;
+      const float lse = (lt > 0.f) ? (m_ref + log2f(lt)) * 0.6931471805599453f : -INFINITY;
+      if (it.direct) a.lse[(size_t)it.loc.b * a.rows_per_req + req_row] = lse;
+      else a.partial_lse[(size_t)it.slot * a.rows_per_req + req_row] = lse;
     }
     if (r == 0 && hw == 0) asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
   }
@@ -750,7 +753,8 @@ __device__ void acc_epilogue(const VerifyArgs& a, const PoolMaps& maps, const It
       named_bar(4 + hc, 128);
       if (store) {
         asm volatile("cp.async.bulk.tensor.3d.global.shared::cta.tile.bulk_group [%0, {%1, %2, %3}], [%4];"
-                     ::"l"(&maps.po), "r"(64 * q), "r"(it.row0), "r"(it.slot), "r"(smem_u32(box))
+                     ::"l"(it.direct ? &maps.fo : &maps.po), "r"(64 * q), "r"(it.row0),
+                       "r"(it.direct ? it.loc.b : it.slot), "r"(smem_u32(box))
                      : "memory");
         asm volatile("cp.async.bulk.commit_group;" ::: "memory");
       }
@@ -768,8 +772,9 @@ __device__ void acc_epilogue(const VerifyArgs& a, const PoolMaps& maps, const It
       if (hc == 0) c->grid_arrived = 2;
     }
   } else if (hc == 0 && it.row0 + r < a.rows_per_req) {
-    for (int d = 0; d < kLatent; ++d)
-      a.partial_o[((size_t)it.slot * a.rows_per_req + it.row0 + r) * kLatent + d] = 0;
+    uint16_t* dst = it.direct ? a.out + ((size_t)it.loc.b * a.rows_per_req + it.row0 + r) * kLatent
+                              : a.partial_o + ((size_t)it.slot * a.rows_per_req + it.row0 + r) * kLatent;
+    for (int d = 0; d < kLatent; ++d) dst[d] = 0;
   }
 }
 
@@ -968,6 +973,12 @@ __device__ void tile_merge(const VerifyArgs& a, const PoolMaps& maps, uint8_t* s
   for (int u = blockIdx.x; u < units; u += gridDim.x, ph ^= 1u) {
     const int b = u / pairs, r0 = 2 * (u - b * pairs);
     if (u != (int)blockIdx.x) tile_merge_slots(a, u, first, count);
+    // A request's only split wrote its final rows itself (unless a wait
+    // expired: then every row is zeroed here).
+    if (count == 1 && !zero) {
+      ph ^= 1u;  // no load this unit: undo the loop's phase step
+      continue;
+    }
     count = zero ? 0 : min(count, D);
     if (tid == 0 && count > 0) {
       // The partials were written by other CTAs' TMA stores, seen through
@@ -1077,6 +1088,9 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(kThreads, 1)
   it.k_begin = have ? it.loc.s * a.chunk_keys : 0;
   it.k_end = have ? min(it.k_begin + a.chunk_keys, it.loc.nkeys) : 0;
   it.ntiles = have ? (it.k_end - it.k_begin + TK - 1) / TK : 0;
+  // A request with one split needs no merge: with the merge in this launch,
+  // its work item writes the final O and LSE rows itself.
+  it.direct = have && a.fused && it.loc.ns == 1;
   // All four CTAs see the same key range; an empty item skips all work but
   // still takes part in the cluster barriers and the pair's TMEM allocation.
 
@@ -1257,6 +1271,15 @@ cudaError_t make_pool_maps(const VerifyArgs& a, PoolMaps* m) {
     const cuuint32_t mbox[3] = {256, 2, (cuuint32_t)a.merge_depth};
     if (enc(&m->pm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, a.partial_o, odims, ostrides, mbox, oes,
             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return cudaErrorInvalidValue;
+  }
+  // Final output as [batch][rows_per_req][512] bf16, for single-split
+  // requests that write their rows directly (rows past a request clipped).
+  if (a.fused) {
+    const cuuint64_t fdims[3] = {(cuuint64_t)kLatent, (cuuint64_t)a.rows_per_req, (cuuint64_t)a.batch};
+    if (enc(&m->fo, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, a.out, fdims, ostrides, obox, oes,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
       return cudaErrorInvalidValue;
   }
