@@ -275,7 +275,6 @@ int run(const ddtree_plan_t* p, const uint16_t* q_latent, const uint16_t* q_rope
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   a.status = reinterpret_cast<uint32_t*>(ws);
   a.grid_done = reinterpret_cast<uint32_t*>(ws + 8);
-  a.grid_go = reinterpret_cast<uint32_t*>(ws + 128);  // its own 128-byte line
   a.partial_lse = reinterpret_cast<float*>(ws + p->off_partial_lse);
   a.partial_o = reinterpret_cast<uint16_t*>(ws + p->off_partial_o);
   a.fused = p->fused_combine;

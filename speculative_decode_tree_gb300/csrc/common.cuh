@@ -40,7 +40,6 @@ struct VerifyArgs {
   uint16_t* partial_o;         // [total_splits, rows_per_req, 512] bf16
   uint32_t* status;            // workspace offset 0
   uint32_t* grid_done;         // workspace offset 8: CTAs finished (fused combine)
-  uint32_t* grid_go;           // workspace offset 128: set by the last arrival (fused combine)
   int64_t pool_rows;           // <= 0: indices unchecked
   float sm_scale;
   int32_t prefix_len_host;

@@ -43,11 +43,12 @@
 //
 // Merge ("Chunk 66.0": partial + reduce): with a one-wave plan the launch is
 // cooperative and the kernel merges its own splits.  Each CTA counts 2 at a
-// grid barrier as soon as its own writes are done (an accumulator's two
-// epilogue store threads once their TMA stores complete; every other CTA
-// before the cluster teardown); the arrival that completes the count raises
-// a flag in a line of its own, which every CTA polls.  Then each CTA merges
-// two rows of a request from TMA tile loads of all their splits.
+// grid barrier (release reductions) as soon as its own writes are done (an
+// accumulator's two epilogue store threads once their TMA stores complete;
+// every other CTA before the cluster teardown), and polls the count.  Then
+// each CTA merges two rows of a request from TMA tile loads of all their
+// splits.  A request with a single split needs no merge: its work item writes
+// the final rows itself and the merge skips it.
 //
 // Every mbarrier wait is bounded; on expiry the kernel sets
 // DDTREE_ST_TIMEOUT, stops issuing work, waits (bounded) for its own
@@ -138,7 +139,7 @@ struct __align__(8) Ctrl {
   uint64_t mma_done;
   uint64_t q_ready;   // scorer: Q latent in TMEM and Q rope in shared memory
   uint64_t qload;     // scorer: the TMA loads of Q (latent staging + rope) landed
-  uint64_t mload[2];  // fused merge: column half h of a unit's partials landed
+  uint64_t mload;     // fused merge: a unit's partials landed
   uint64_t wait_ns;        // bound of the waits (the caller's, default 2 s)
   uint32_t tmem_base;
   uint32_t abort;
@@ -697,16 +698,6 @@ __device__ void scorer(const VerifyArgs& a, const PoolMaps& maps, const Item& it
   }
 }
 
-// Count n arrivals at the fused merge's grid barrier (every CTA counts 2).
-// Release: the caller's writes (and what it has seen) are visible to whoever
-// sees the count complete.  The arrival that completes it raises the flag the
-// other CTAs poll, which lives in its own line, apart from the atomics.
-__device__ __forceinline__ void grid_arrive(const VerifyArgs& a, uint32_t n) {
-  uint32_t old;
-  asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], %2;" : "=r"(old) : "l"(a.grid_done), "r"(n) : "memory");
-  if (old + n == 2u * gridDim.x) asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(a.grid_go), "r"(1u) : "memory");
-}
-
 // ------------------------------------------------------------ accumulator
 // Accumulator epilogue: O_s = O / l as bf16 rows of the workspace, by eight
 // warps -- 4..7 (after the tile loop) write columns 0..255, 12..15 columns
@@ -768,7 +759,7 @@ __device__ void acc_epilogue(const VerifyArgs& a, const PoolMaps& maps, const It
       // This half of the CTA's partial rows is in global memory: it counts
       // itself in at the merge's grid barrier now (release), instead of after
       // the CTA's teardown.  Both halves always do, so the CTA owes none later.
-      if (a.fused) grid_arrive(a, 1);
+      if (a.fused) asm volatile("red.release.gpu.global.add.u32 [%0], 1;" ::"l"(a.grid_done) : "memory");
       if (hc == 0) c->grid_arrived = 2;
     }
   } else if (hc == 0 && it.row0 + r < a.rows_per_req) {
@@ -984,13 +975,12 @@ __device__ void tile_merge(const VerifyArgs& a, const PoolMaps& maps, uint8_t* s
       // The partials were written by other CTAs' TMA stores, seen through
       // the grid barrier (generic proxy); these loads are async proxy.
       asm volatile("fence.proxy.async.global;" ::: "memory");
-      for (int h = 0; h < 2; ++h) {
-        mbar_arrive_expect_tx(&c->mload[h], box_bytes);
+      mbar_arrive_expect_tx(&c->mload, 2 * box_bytes);
+      for (int h = 0; h < 2; ++h)
         asm volatile(
             "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], [%5];"
-            ::"r"(smem_u32(sm + h * box_bytes)), "l"(&maps.pm), "r"(256 * h), "r"(r0), "r"(first), "r"(smem_u32(&c->mload[h]))
+            ::"r"(smem_u32(sm + h * box_bytes)), "l"(&maps.pm), "r"(256 * h), "r"(r0), "r"(first), "r"(smem_u32(&c->mload))
             : "memory");
-      }
     }
     if (warp < 2) {  // warp w: the weights of row r0 + w (lane j: splits j, j + 32)
       const int row = r0 + warp;
@@ -1021,40 +1011,38 @@ __device__ void tile_merge(const VerifyArgs& a, const PoolMaps& maps, uint8_t* s
       if (lane == 0) rowl[warp] = l > 0.f ? m + logf(l) : -INFINITY;
     }
     __syncthreads();
-    // thread: row r0 + (tid >> 8), columns 2 (tid & 255) .. + 1, of column
-    // half h (uniform in a warp); it waits only for its half's box.
+    bool ok = true;
+    if (count > 0) ok = mbar_wait(&c->mload, ph, a.wait_ns);
+    if (!ok && tid == 0) atomicOr(a.status, DDTREE_ST_TIMEOUT);
+    // thread: row r0 + (tid >> 8), columns 2 (tid & 255) .. + 1
     const int rr = tid >> 8, col = 2 * (tid & 255);
     const int row = r0 + rr;
-    const int h = col >> 8;
-    bool ok = true;
-    if (count > 0) ok = mbar_wait(&c->mload[h], ph, a.wait_ns);
-    if (!ok && lane == 0) atomicOr(a.status, DDTREE_ST_TIMEOUT);
     if (row < a.rows_per_req) {
-      const uint8_t* src = sm + h * box_bytes + rr * 512 + (col & 255) * 2;  // split s at + 1 KB s
-      // Eight splits per step (eight independent loads, two 16-byte weight
-      // loads) into two sums of each column.
+      const int h = col >> 8;
+      const uint8_t* src = sm + h * box_bytes + rr * 512 + (col & 255) * 2;
+      // Four splits per step into two sums of each column (the loads of a
+      // step are independent; the chains are half as long).
       float acc0 = 0.f, acc1 = 0.f, acc2 = 0.f, acc3 = 0.f;
       if (ok) {
         const float* wr = wgt + 64 * rr;
         int s = 0;
 #pragma unroll 1
-        for (; s + 8 <= count; s += 8) {
-          const float4 wa = *reinterpret_cast<const float4*>(wr + s);
-          const float4 wb = *reinterpret_cast<const float4*>(wr + s + 4);
-          const float w[8] = {wa.x, wa.y, wa.z, wa.w, wb.x, wb.y, wb.z, wb.w};
-          uint32_t x[8];
+        for (; s + 4 <= count; s += 4) {
+          const float4 w = *reinterpret_cast<const float4*>(wr + s);  // one load for four weights
+          uint32_t x[4];
 #pragma unroll
-          for (int e = 0; e < 8; ++e) x[e] = *reinterpret_cast<const uint32_t*>(src + (s + e) * 1024);
-#pragma unroll
-          for (int e = 0; e < 8; e += 2) {
-            acc0 = fmaf(w[e], bf16_lo(x[e]), acc0);
-            acc1 = fmaf(w[e], bf16_hi(x[e]), acc1);
-            acc2 = fmaf(w[e + 1], bf16_lo(x[e + 1]), acc2);
-            acc3 = fmaf(w[e + 1], bf16_hi(x[e + 1]), acc3);
-          }
+          for (int e = 0; e < 4; ++e) x[e] = *reinterpret_cast<const uint32_t*>(src + (size_t)(s + e) * 1024);
+          acc0 = fmaf(w.x, bf16_lo(x[0]), acc0);
+          acc1 = fmaf(w.x, bf16_hi(x[0]), acc1);
+          acc2 = fmaf(w.y, bf16_lo(x[1]), acc2);
+          acc3 = fmaf(w.y, bf16_hi(x[1]), acc3);
+          acc0 = fmaf(w.z, bf16_lo(x[2]), acc0);
+          acc1 = fmaf(w.z, bf16_hi(x[2]), acc1);
+          acc2 = fmaf(w.w, bf16_lo(x[3]), acc2);
+          acc3 = fmaf(w.w, bf16_hi(x[3]), acc3);
         }
         for (; s < count; ++s) {
-          const uint32_t x = *reinterpret_cast<const uint32_t*>(src + s * 1024);
+          const uint32_t x = *reinterpret_cast<const uint32_t*>(src + (size_t)s * 1024);
           acc0 = fmaf(wr[s], bf16_lo(x), acc0);
           acc1 = fmaf(wr[s], bf16_hi(x), acc1);
         }
@@ -1122,7 +1110,7 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(kThreads, 1)
     mbar_init(&c->mma_done, 2);  // two MMA issuers per pair
     mbar_init(&c->q_ready, 8);
     mbar_init(&c->qload, 1);
-    for (int i = 0; i < 2; ++i) mbar_init(&c->mload[i], 1);
+    mbar_init(&c->mload, 1);
     c->abort = 0;
     c->grid_arrived = 0;
     c->wait_ns = a.wait_ns;
@@ -1169,7 +1157,7 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(kThreads, 1)
     // ordered before this thread by the barrier above, are visible to
     // whoever sees the count.
     const uint32_t late = 2u - c->grid_arrived;
-    if (late) grid_arrive(a, late);
+    if (late) asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(a.grid_done), "r"(late) : "memory");
   }
   // Tensor-core work writing this CTA's TMEM must be finished before it is freed.
   if (warp == 3 && work) mbar_wait_cluster(&c->mma_done, 0, kDrainNs);
@@ -1192,12 +1180,10 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(kThreads, 1)
     if (tid == 0) {
       uint64_t deadline = 0;
       bool ok = true;
-      // Relaxed polls of the flag the last arrival raises; one acquire fence
-      // once it is seen.
       for (uint32_t spin = 1;; ++spin) {
         uint32_t v;
-        asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(a.grid_go) : "memory");
-        if (v != 0u) break;
+        asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(a.grid_done) : "memory");
+        if (v >= 2u * gridDim.x) break;
         if (spin == 4u) {
           deadline = global_timer_ns() + a.wait_ns;
         } else if (spin > 4u && (spin & 7u) == 0u && global_timer_ns() > deadline) {
@@ -1205,10 +1191,9 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(kThreads, 1)
           break;
         }
       }
-      asm volatile("fence.acq_rel.gpu;" ::: "memory");
       if (!ok) atomicOr(a.status, DDTREE_ST_TIMEOUT);
       uint32_t st;
-      asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(st) : "l"(a.status) : "memory");
+      asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(st) : "l"(a.status) : "memory");
       c->merge_zero = (!ok || (st & DDTREE_ST_TIMEOUT)) ? 1u : 0u;
     }
     __syncthreads();

@@ -131,7 +131,6 @@ extern "C" int ddtree_verify_mla_noalloc(const ddtree_bf16_t* q_latent, const dd
   uint8_t* ws = static_cast<uint8_t*>(scratch);
   a.status = reinterpret_cast<uint32_t*>(ws);
   a.grid_done = reinterpret_cast<uint32_t*>(ws + 8);
-  a.grid_go = reinterpret_cast<uint32_t*>(ws + 128);  // its own 128-byte line
   a.partial_lse = reinterpret_cast<float*>(ws + plan.off_partial_lse);
   a.partial_o = reinterpret_cast<uint16_t*>(ws + plan.off_partial_o);
   a.fused = plan.fused_combine;
