@@ -286,13 +286,16 @@ __device__ __forceinline__ int* ring_tile(uint8_t* sm, int t) {
 
 // Loader warp: tile j's 128 indices (invalid ones -> -1, flagged) into ring
 // slot j % NIDX, with the tile's first index and whether it is one run.  The
-// loads of four tiles are in flight together, each at an address clamped into
+// loads of kIdxBatch tiles go out together, each at an address clamped into
 // the work item's keys (the keys past its end are masked when stored): a load
 // under a condition feeding a select would wait for each in turn.  The first
-// four tiles' loads are issued while the CTA is still being set up.  (An L2
-// prefetch of the rows from this warp measured slower: the prefetch
-// instructions held the loader back.)
-constexpr int kIdxBatch = 4;
+// batch is issued while the CTA is still being set up.  One tile per batch
+// measured fastest (batches of 1 / 2 / 4 / 8 tiles: 48.0–49.9 / 49.9 / 50.2 /
+// 54.0 us on the 65k workload, 23.3 / 23.3 / 25.5 / 29.5 us on a 4k prefix):
+// the loader runs ahead through the ring anyway, and a smaller batch reaches
+// the first tile's indices sooner.  (An L2 prefetch of the rows from this
+// warp measured slower: the prefetch instructions held the loader back.)
+constexpr int kIdxBatch = 1;
 __device__ __forceinline__ void index_batch_load(const VerifyArgs& a, const Item& it, int j0, int lane,
                                                  int (&v)[kIdxBatch][4]) {
 #pragma unroll
