@@ -120,7 +120,7 @@ def _peaks():
 # when it was taken (profiles/ has the summaries and commands).  Any other
 # version of the source reports null.
 TRAFFIC = {
-    "k_partial_tc2.cu": ("374f0ad18b3abfb39c310fada18ca868555c1786", 76242176 + 2660096),
+    "k_partial_tc2.cu": ("53337ef9fab02683862ab9e5d5950e4d1e46ac7e", 76216064 + 2440704),
     "k_accept.cu": ("016411fbe872d42040beebcfdb04b0f2d27eef9e", 8556032),
     "k_mask.cu": ("35de2ba635e46a78af91ca088bc100827946414a", 2114000),
     # mark + check + copy of one relocate_long call
