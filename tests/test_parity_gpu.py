@@ -73,7 +73,23 @@ def _random_shapes(n: int, seed: int):
     return shapes
 
 
-RANDOM = _random_shapes(12, seed=20261203) + [
+def _wide_shapes(n: int, seed: int):
+    """Seeded draws with many heads and few nodes: three to eight row tiles,
+    so the quad kernel runs several row pairs of one split side by side."""
+    import random
+    r = random.Random(seed)
+    shapes = []
+    for _ in range(n):
+        batch = r.randint(1, 3)
+        H = r.choice([32, 64, 128])
+        T = r.choice([t for t in (2, 3, 4, 5, 8, 12, 16, 24, 32) if 256 < t * H <= 1024])
+        prefixes = [r.choice([0, r.randint(1, 500), r.randint(500, 3000)]) for _ in range(batch)]
+        shapes.append((batch, T, H, prefixes, r.choice(["chain", "uniform", "bounded"]),
+                       r.choice(["sample", "interleaved"])))
+    return shapes
+
+
+RANDOM = _random_shapes(12, seed=20261203) + _wide_shapes(6, seed=1203) + [
     # longer prefixes: several splits per request, fused merge over many of them
     (2, 16, 8, [20000, 9000], "uniform", "interleaved"),
     (1, 32, 8, [30000], "bounded", "sample"),
@@ -81,7 +97,7 @@ RANDOM = _random_shapes(12, seed=20261203) + [
 
 
 @pytest.mark.parametrize("kernel", [None, B.DDTREE_KERNEL_TC2], ids=["auto", "tc2"])
-@pytest.mark.parametrize("shape", RANDOM, ids=[f"B{s[0]}_T{s[1]}_H{s[2]}_{s[4]}_{s[5]}" for s in RANDOM])
+@pytest.mark.parametrize("shape", RANDOM, ids=[f"B{s[0]}_T{s[1]}_H{s[2]}_P{sum(s[3])}_{s[4]}_{s[5]}" for s in RANDOM])
 def test_random_plans_match_oracle(shape, kernel):
     batch, T, H, prefixes, tree, mode = shape
     pool_rows = max(1024, 2 * sum(p + T for p in prefixes))
