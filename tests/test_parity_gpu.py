@@ -109,6 +109,21 @@ def test_random_plans_match_oracle(shape, kernel):
 
 
 @pytest.mark.parametrize("kernel", KERNELS)
+def test_rows_at_both_ends_of_the_pool(kernel):
+    """Keys in the pool's first and last rows: four whole tiles of one run that
+    ends at the last row (the quad kernel loads such tiles as 2-D TMA boxes),
+    then row 0 and the last row again among scattered rows."""
+    T, H, P, pool_rows = 16, 8, 1000, 4096
+    inp = make_inputs("ends", batch=1, n_heads=H, prefixes=[P], n_nodes=T, tree="uniform",
+                      pool_rows=pool_rows, index_mode="sample", seed=77)
+    inp.kv_indices[:512] = torch.arange(pool_rows - 512, pool_rows, dtype=torch.int32)
+    inp.kv_indices[512] = 0
+    inp.kv_indices[700] = pool_rows - 1
+    inp.kv_indices[P + T - 1] = pool_rows - 1
+    _compare_all(inp, kernel, f"pool ends, kernel {kernel}")
+
+
+@pytest.mark.parametrize("kernel", KERNELS)
 def test_ragged_batch_matches_oracle(kernel):
     prefixes = [0, 5, 777, 64, 1, 2049, 31, 300]
     inp = make_inputs("ragged", batch=8, n_heads=4, prefixes=prefixes, n_nodes=12, tree="uniform",
